@@ -1,0 +1,362 @@
+/*
+ * oracle.c -- the CPU oracle for the attention forward and the Sage prepare.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; it is used by tests/, by the smoke check and by the benchmark's
+ * CPU-baseline leg.  It shares no code, header, table or constant generator
+ * with the CUDA library.
+ *
+ * It is deliberately plain and slow:
+ *   - attention is the textbook definition O = softmax(scale * Q K^T) V
+ *     evaluated per query row in FP64 (ai-infra handbook, "Kernel
+ *     acceleration: attention, compilation and fusion", section "Attention:
+ *     from O(N^2) memory to blocks", the `naive` form); no tiling, no online
+ *     softmax;
+ *   - the Sage prepare is the quantisation of the aiter pull request
+ *     "gfx1201_sage_prepare / gfx1201_sage_attention" (commit message of
+ *     gfx1201_sage_prepare; Technical Details), written step by step in IEEE
+ *     binary32 with round-to-nearest-even and no fused multiply-add (this file
+ *     must be compiled with -ffp-contract=off and without fast-math).  Where
+ *     that page leaves a step open, the reading taken is written beside it.
+ *
+ * Tensors arrive as BF16 bit patterns (uint16) in contiguous [B, S, H, D]
+ * order, D = 128 for everything but the attention definition, which takes any D.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- scalars */
+
+static float f32_from_bits(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t bits_from_f32(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* BF16 is the upper half of a binary32: widening is exact. */
+float oracle_bf16_to_f32(uint16_t b) { return f32_from_bits((uint32_t)b << 16); }
+
+/* Value of a BF16 magnitude pattern (sign bit clear) as a double, treating the
+ * pattern one past the largest finite value as 2^128 (the next step of the
+ * exponent scale) so that rounding near the top behaves like unbounded RNE. */
+static double bf16_mag_value(uint32_t pat) {
+    if (pat >= 0x7f80u) return ldexp(1.0, 128);
+    return (double)f32_from_bits(pat << 16);
+}
+
+/* Round a finite binary32 to BF16, nearest, ties to the even pattern.
+ * Brute force on the two neighbours: the pattern obtained by truncation and
+ * the next one up in magnitude. */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u = bits_from_f32(f);
+    uint32_t sign = u & 0x80000000u;
+    uint32_t mag = u & 0x7fffffffu;
+    if (mag > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);      /* NaN stays NaN */
+    if (mag == 0x7f800000u) return (uint16_t)(u >> 16);                   /* +-inf */
+    double a = fabs((double)f);
+    uint32_t lo = mag >> 16, hi = lo + 1;
+    double dl = a - bf16_mag_value(lo), dh = bf16_mag_value(hi) - a;
+    uint32_t pick;
+    if (dl < dh) pick = lo;
+    else if (dh < dl) pick = hi;
+    else pick = (lo & 1u) ? hi : lo;
+    return (uint16_t)((sign >> 16) | pick);
+}
+
+/* FP8 e4m3 ("e4m3fn"): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, no infinities, S.1111.111 is NaN.  Largest finite magnitude is
+ * 1.75 * 2^8 = 448, smallest subnormal 2^-9. */
+double oracle_e4m3_decode(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = m * ldexp(1.0, -9);
+    else v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return s ? -v : v;
+}
+
+/* The 127 finite non-negative e4m3 magnitudes, indexed by code (they increase
+ * with the code), filled once from the definition above. */
+static double e4m3_mag[127];
+static int e4m3_ready = 0;
+static void e4m3_init(void) {
+    if (e4m3_ready) return;
+    for (int c = 0; c < 127; c++) e4m3_mag[c] = oracle_e4m3_decode((uint8_t)c);
+    e4m3_ready = 1;
+}
+
+/* Encode a finite binary32 as e4m3: round to nearest, ties to the even code,
+ * magnitudes at or above 448 saturate to 448 ("satfinite").  The sign of the
+ * input is kept, zero included.  Bisection finds the two neighbouring finite
+ * magnitudes; the nearer one wins, a tie goes to the even code. */
+uint8_t oracle_e4m3_encode(float x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (isnan(x)) return 0x7f;
+    e4m3_init();
+    if (a >= 448.0) return sign | 126;
+    int lo = 0, hi = 126;              /* invariant: mag[lo] <= a < mag[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (e4m3_mag[mid] <= a) lo = mid; else hi = mid;
+    }
+    double dl = a - e4m3_mag[lo];
+    double dh = e4m3_mag[hi] - a;
+    int pick;
+    if (dl < dh) pick = lo;
+    else if (dh < dl) pick = hi;
+    else pick = (lo & 1) ? hi : lo;
+    return sign | (uint8_t)pick;
+}
+
+void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(x[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t* c, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_decode(c[i]);
+}
+void oracle_f32_to_bf16_array(const float* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_f32_to_bf16(x[i]);
+}
+
+/* ------------------------------------------------------------- attention */
+
+/*
+ * O[b, s, h, :] = sum_j w_j V[b, j, h, :] / sum_j w_j,
+ *   w_j = exp(t_j - max_j t_j),  t_j = scale * <Q[b, s, h, :], K[b, j, h, :]>,
+ * all in FP64 from the exactly widened BF16 inputs.  Subtracting the row
+ * maximum only keeps exp() finite; it cancels in the ratio.
+ *
+ * rows: optional list of flattened query rows r = (b*S + s)*H + h; NULL means
+ * every row in order.  out: [n_rows, D] doubles.
+ */
+void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      int B, int S, int H, int D, double scale,
+                      const int64_t* rows, int64_t n_rows, double* out, int nthreads) {
+    int64_t total = rows ? n_rows : (int64_t)B * S * H;
+    (void)nthreads;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        double* t = (double*)malloc(sizeof(double) * (size_t)S);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < total; i++) {
+            int64_t r = rows ? rows[i] : i;
+            int64_t h = r % H, s = (r / H) % S, b = r / ((int64_t)H * S);
+            const uint16_t* qrow = q + ((b * S + s) * H + h) * D;
+            for (int d = 0; d < D; d++) qd[d] = (double)oracle_bf16_to_f32(qrow[d]);
+            double tmax = -INFINITY;
+            for (int64_t j = 0; j < S; j++) {
+                const uint16_t* krow = k + ((b * S + j) * H + h) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; d++) dot += qd[d] * (double)oracle_bf16_to_f32(krow[d]);
+                t[j] = scale * dot;
+                if (t[j] > tmax) tmax = t[j];
+            }
+            double wsum = 0.0;
+            for (int d = 0; d < D; d++) acc[d] = 0.0;
+            for (int64_t j = 0; j < S; j++) {
+                double w = exp(t[j] - tmax);
+                const uint16_t* vrow = v + ((b * S + j) * H + h) * D;
+                wsum += w;
+                for (int d = 0; d < D; d++) acc[d] += w * (double)oracle_bf16_to_f32(vrow[d]);
+            }
+            for (int d = 0; d < D; d++) out[i * D + d] = acc[d] / wsum;
+        }
+        free(t); free(qd); free(acc);
+    }
+}
+
+/* ------------------------------------------------- Sage prepare: RMSNorm */
+
+/*
+ * RMSNorm of one 128-channel head row, "rounded like the eager PyTorch BF16
+ * sequence" (aiter pull request, gfx1201_sage_prepare commit message):
+ *   y   = bf16( x * r ),   r = 1 / sqrt( mean(x^2) + eps )
+ *   out = bf16( y * w )
+ * with x widened from BF16 and every operation an IEEE binary32 operation.
+ *
+ * Reading (the page does not give a summation order): the sum of squares is
+ * taken in sixteen partial sums, partial L = x[8L]^2 + ... + x[8L+7]^2 added
+ * left to right, then combined pairwise like an XOR butterfly over the sixteen
+ * partials with distances 8, 4, 2, 1.  The mean is that sum times 1/128 (exact,
+ * a power of two); sqrt and the reciprocal are each rounded once.
+ */
+static void rmsnorm_row(const uint16_t* x, const uint16_t* w, float eps, uint16_t* out) {
+    float part[16];
+    for (int L = 0; L < 16; L++) {
+        float acc = 0.0f;
+        for (int i = 0; i < 8; i++) {
+            float xi = oracle_bf16_to_f32(x[8 * L + i]);
+            float sq = xi * xi;
+            acc = acc + sq;
+        }
+        part[L] = acc;
+    }
+    for (int dist = 8; dist >= 1; dist >>= 1) {
+        float nxt[16];
+        for (int L = 0; L < 16; L++) nxt[L] = part[L] + part[L ^ dist];
+        memcpy(part, nxt, sizeof(part));
+    }
+    float sumsq = part[0];
+    float ms = sumsq * (1.0f / 128.0f);
+    float den = sqrtf(ms + eps);
+    float r = 1.0f / den;
+    for (int c = 0; c < 128; c++) {
+        float xc = oracle_bf16_to_f32(x[c]);
+        uint16_t y = oracle_f32_to_bf16(xc * r);
+        float yw = oracle_bf16_to_f32(y) * oracle_bf16_to_f32(w[c]);
+        out[c] = oracle_f32_to_bf16(yw);
+    }
+}
+
+/*
+ * Rotate-half RoPE on the first rope_dim channels of one head row at sequence
+ * position s (aiter pull request, gfx1201_sage_prepare commit message:
+ * "rotate-half RoPE (rope_dim 32/64/96/128)").  With h = rope_dim / 2:
+ *   rot[c] = -x[c + h] for c < h,   rot[c] = x[c - h] for h <= c < rope_dim
+ *   out[c] = bf16( bf16(x[c] * cos[s, c]) + bf16(rot[c] * sin[s, c]) )
+ * which is the eager BF16 sequence x*cos + rotate_half(x)*sin (each product
+ * and the sum rounded to BF16).  Channels >= rope_dim pass through.
+ */
+static void rope_row(const uint16_t* x, const uint16_t* cosr, const uint16_t* sinr, int rope_dim,
+                     uint16_t* out) {
+    int h = rope_dim / 2;
+    for (int c = 0; c < 128; c++) {
+        if (c >= rope_dim) { out[c] = x[c]; continue; }
+        float xc = oracle_bf16_to_f32(x[c]);
+        float rot = (c < h) ? -oracle_bf16_to_f32(x[c + h]) : oracle_bf16_to_f32(x[c - h]);
+        uint16_t a = oracle_f32_to_bf16(xc * oracle_bf16_to_f32(cosr[c]));
+        uint16_t b = oracle_f32_to_bf16(rot * oracle_bf16_to_f32(sinr[c]));
+        out[c] = oracle_f32_to_bf16(oracle_bf16_to_f32(a) + oracle_bf16_to_f32(b));
+    }
+}
+
+/*
+ * Optional fused pre-processing of Q or K: RMSNorm (when w != NULL), then RoPE
+ * (when rope_dim > 0).  x, out: contiguous [B, S, H, 128]; cos/sin: [S, rope_dim].
+ */
+void oracle_norm_rope(const uint16_t* x, int B, int S, int H, const uint16_t* w, float eps,
+                      const uint16_t* cos_t, const uint16_t* sin_t, int rope_dim, uint16_t* out) {
+    int64_t nrow = (int64_t)B * S * H;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrow; r++) {
+        int64_t s = (r / H) % S;
+        uint16_t tmp[128];
+        const uint16_t* src = x + r * 128;
+        if (w) { rmsnorm_row(src, w, eps, tmp); src = tmp; }
+        if (rope_dim > 0) {
+            uint16_t tmp2[128];
+            rope_row(src, cos_t + s * rope_dim, sin_t + s * rope_dim, rope_dim, tmp2);
+            memcpy(out + r * 128, tmp2, sizeof(tmp2));
+        } else {
+            memcpy(out + r * 128, src, 128 * sizeof(uint16_t));
+        }
+    }
+}
+
+/* ---------------------------------------------- Sage prepare: Q/K to INT8 */
+
+/*
+ * "Q/K -> INT8 with one FP32 scale per (batch, head, 32-row block), Q carrying
+ * softmax_scale * log2(e)" (aiter pull request, Technical Details).
+ *
+ * Readings: symmetric quantisation with the block's absolute maximum a over
+ * its valid rows (rows < S):
+ *   inv = 127 / a,  code = clamp(rint(x * inv), -127, 127)   (ties to even)
+ *   scale = a / 127                    for K  (scale_mult = 1)
+ *   scale = (a / 127) * scale_mult     for Q  (scale_mult = fl32(softmax_scale * log2 e))
+ * a == 0 gives all-zero codes and scale 0.  The INT8 bytes therefore depend on
+ * the tensor alone; the softmax factor lives in Q's scale.
+ * Output layout [B, H, S_pad, 128] (row-major); rows in [S, S_pad) are zero and
+ * the scales of blocks wholly beyond S are zero.  scales: [B, H, S_pad / 32].
+ */
+void oracle_quant_qk(const uint16_t* x, int B, int S, int H, int64_t S_pad, float scale_mult,
+                     int8_t* codes, float* scales) {
+    int64_t nblk = S_pad / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < H; h++) {
+            for (int64_t j = 0; j < nblk; j++) {
+                int64_t r0 = 32 * j, r1 = r0 + 32 < S ? r0 + 32 : S;
+                float a = 0.0f;
+                for (int64_t s = r0; s < r1; s++)
+                    for (int c = 0; c < 128; c++) {
+                        float xv = fabsf(oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]));
+                        if (xv > a) a = xv;
+                    }
+                float inv = (a > 0.0f) ? 127.0f / a : 0.0f;
+                for (int64_t s = r0; s < r0 + 32; s++) {
+                    int8_t* dst = codes + (((int64_t)b * H + h) * S_pad + s) * 128;
+                    for (int c = 0; c < 128; c++) {
+                        if (s >= S || a == 0.0f) { dst[c] = 0; continue; }
+                        float xv = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                        float t = xv * inv;
+                        float rq = rintf(t);
+                        if (rq > 127.0f) rq = 127.0f;
+                        if (rq < -127.0f) rq = -127.0f;
+                        dst[c] = (int8_t)rq;
+                    }
+                }
+                float sc = 0.0f;
+                if (a > 0.0f) {
+                    sc = a / 127.0f;
+                    sc = sc * scale_mult;
+                }
+                scales[((int64_t)b * H + h) * nblk + j] = sc;
+            }
+        }
+    }
+}
+
+/* ----------------------------------------------- Sage prepare: V to e4m3 */
+
+/*
+ * "V -> FP8 e4m3, transposed to [B, H, 128, S_pad], one FP32 scale per
+ * channel" (aiter pull request, Technical Details).
+ *
+ * Readings: one scale per (batch, head, channel) from the channel's absolute
+ * maximum a over all valid positions s < S; inv = 448 / a (448 being the
+ * largest e4m3 value); code = e4m3_rn_satfinite(v * inv); scale = a / 448.
+ * a == 0 gives zero codes and scale 0.  Positions in [S, S_pad) are zero.
+ * codes: [B, H, 128, S_pad]; scales: [B, H, 128].
+ */
+void oracle_quant_v(const uint16_t* x, int B, int S, int H, int64_t S_pad, uint8_t* codes, float* scales) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < H; h++) {
+            for (int c = 0; c < 128; c++) {
+                float a = 0.0f;
+                for (int64_t s = 0; s < S; s++) {
+                    float xv = fabsf(oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]));
+                    if (xv > a) a = xv;
+                }
+                float inv = (a > 0.0f) ? 448.0f / a : 0.0f;
+                uint8_t* dst = codes + (((int64_t)b * H + h) * 128 + c) * S_pad;
+                for (int64_t s = 0; s < S_pad; s++) {
+                    if (s >= S || a == 0.0f) { dst[s] = 0; continue; }
+                    float xv = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                    float t = xv * inv;
+                    dst[s] = oracle_e4m3_encode(t);
+                }
+                scales[((int64_t)b * H + h) * 128 + c] = (a > 0.0f) ? a / 448.0f : 0.0f;
+            }
+        }
+    }
+}
+
+void oracle_init(void) { e4m3_init(); }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
