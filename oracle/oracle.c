@@ -183,25 +183,25 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * with x widened from BF16 and every operation an IEEE binary32 operation.
  *
  * Reading (the page does not give a summation order): the sum of squares is
- * taken in sixteen partial sums, partial L = x[8L]^2 + ... + x[8L+7]^2 added
- * left to right, then combined pairwise like an XOR butterfly over the sixteen
- * partials with distances 8, 4, 2, 1.  The mean is that sum times 1/128 (exact,
+ * taken in eight partial sums, partial L = x[16L]^2 + ... + x[16L+15]^2 added
+ * left to right, then combined pairwise like an XOR butterfly over the eight
+ * partials with distances 4, 2, 1.  The mean is that sum times 1/128 (exact,
  * a power of two); sqrt and the reciprocal are each rounded once.
  */
 static void rmsnorm_row(const uint16_t* x, const uint16_t* w, float eps, uint16_t* out) {
-    float part[16];
-    for (int L = 0; L < 16; L++) {
+    float part[8];
+    for (int L = 0; L < 8; L++) {
         float acc = 0.0f;
-        for (int i = 0; i < 8; i++) {
-            float xi = oracle_bf16_to_f32(x[8 * L + i]);
+        for (int i = 0; i < 16; i++) {
+            float xi = oracle_bf16_to_f32(x[16 * L + i]);
             float sq = xi * xi;
             acc = acc + sq;
         }
         part[L] = acc;
     }
-    for (int dist = 8; dist >= 1; dist >>= 1) {
-        float nxt[16];
-        for (int L = 0; L < 16; L++) nxt[L] = part[L] + part[L ^ dist];
+    for (int dist = 4; dist >= 1; dist >>= 1) {
+        float nxt[8];
+        for (int L = 0; L < 8; L++) nxt[L] = part[L] + part[L ^ dist];
         memcpy(part, nxt, sizeof(part));
     }
     float sumsq = part[0];
