@@ -1,0 +1,184 @@
+/*
+ * sageattn.h -- C ABI of the GB300 (sm_103a) attention forward library.
+ *
+ * Three operations, each defined on the pages this library restates:
+ *
+ *   attn_fwd_bf16   O = softmax(scale * Q K^T) V, non-causal self-attention,
+ *                   BF16 [B, S, H, 128] in and out, computed tile by tile with
+ *                   an online softmax so the S x S score matrix is never
+ *                   stored.  (ai-infra handbook, "Kernel acceleration:
+ *                   attention, compilation and fusion", section "Attention:
+ *                   from O(N^2) memory to blocks"; the RDNA2 DiT flash kernel
+ *                   note, Contribution.)
+ *   sage_prepare    the input stage of the SageAttention-style forward: Q/K to
+ *                   INT8 with one FP32 scale per (batch, head, 32-row block),
+ *                   Q's scale carrying softmax_scale * log2(e); V to FP8 e4m3
+ *                   transposed to [B, H, 128, S_pad] with one FP32 scale per
+ *                   channel; optionally QK RMSNorm and rotate-half RoPE first,
+ *                   rounded like the eager PyTorch BF16 sequence.  (aiter pull
+ *                   request "gfx1201_sage_prepare / gfx1201_sage_attention",
+ *                   commit message of gfx1201_sage_prepare; Technical Details.)
+ *   sage_attn_fwd   the attention kernel alone on prepared tensors: Q K^T on
+ *                   the INT8 codes, P V with P and V in FP8 e4m3, FP32
+ *                   accumulation, online softmax, BF16 output.  (Same pull
+ *                   request, commit message of gfx1201_sage_attention:
+ *                   "gfx1201_sage_attention_fwd runs the kernel alone on
+ *                   prepared tensors".)
+ *
+ * Conventions shared by every call
+ *   - D (head dimension) must be 128; B, S, H >= 1.
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller; the library never allocates, frees or keeps them.
+ *     Every pointer must be 16-byte aligned.
+ *   - BF16 tensors are addressed as [B, S, H, 128] with element strides given
+ *     as int64_t str[3] = {stride_b, stride_s, stride_h}; the channel stride is
+ *     1.  Each stride must be a positive multiple of 8 elements (16 bytes);
+ *     the stride of a dimension of extent 1 is ignored.  Views such as the
+ *     [B, H, S, D] storage seen through its [B, S, H, D] permutation are
+ *     accepted as they are.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and enqueue kernels only.  Argument errors are found on
+ *     the host before anything is enqueued.
+ *   - Each call returns ATTN_OK or an error; attn_last_error() gives the
+ *     message of the calling thread's last failed call.
+ *   - Device-side pipeline waits are bounded (about 2 s).  A wait that runs
+ *     out makes its kernel stop early and records the fact in a device error
+ *     word; attn_get_device_status() reports and clears it.
+ *   - The library runs on sm_103 devices only; elsewhere every call returns
+ *     ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef SAGEATTN_H_
+#define SAGEATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null pointer, bad extent, bad stride, bad option */
+  ATTN_ERR_ALIGNMENT = 2,      /* pointer not 16-byte aligned, stride not a multiple of 8 elements */
+  ATTN_ERR_UNSUPPORTED = 3,    /* not an sm_103 device, or D != 128 */
+  ATTN_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (message has the CUDA error) */
+  ATTN_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up on a bounded wait (from attn_get_device_status) */
+} attn_status;
+
+/*
+ * attn_fwd_bf16 -- O = softmax(softmax_scale * Q K^T) V over all S keys.
+ *   q, k, v : const BF16 [B, S, H, 128], strides q_str/k_str/v_str
+ *   o       : BF16 [B, S, H, 128] output, stride o_str; must not overlap q/k/v
+ *   softmax_scale : any finite float (1/sqrt(128) for the usual attention)
+ * Result is FP32-accumulated and rounded to BF16 once.  No mask, no causal
+ * variant, no dropout.
+ */
+ATTN_API attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int H, int D,
+                          const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                          const int64_t o_str[3], float softmax_scale, attn_stream_t stream);
+
+/* sage_padded_len -- S rounded up to a multiple of 128: the smallest valid S_pad. */
+ATTN_API int64_t sage_padded_len(int64_t S);
+
+/*
+ * sage_prepare_workspace_size -- bytes of device scratch sage_prepare needs
+ * for B x H heads (the per-channel V maxima, reduced across the sequence
+ * before any V element can be encoded).  The caller allocates it.
+ */
+ATTN_API size_t sage_prepare_workspace_size(int B, int H);
+
+/*
+ * sage_prepare -- quantise Q, K and V for sage_attn_fwd.
+ *   q, k, v    : const BF16 [B, S, H, 128] with strides q_str/k_str/v_str
+ *   softmax_scale : folded, with log2(e), into q_scale:
+ *                   c = (float)((double)softmax_scale * log2(e))
+ *   q_norm_w, k_norm_w : BF16 [128] RMSNorm weights, both given or both NULL.
+ *                   When given, each 128-channel head row x of Q (resp. K) is
+ *                   replaced by bf16(bf16(x * r) * w), r = 1/sqrt(mean(x^2) + rms_eps),
+ *                   all in binary32 (sum of squares: eight partial sums over
+ *                   channels [16L, 16L+16) added left to right, combined
+ *                   pairwise like an XOR butterfly at distances 4, 2, 1; sqrt
+ *                   and the division each rounded once).
+ *   rope_cos, rope_sin : BF16 [S, rope_dim] tables (contiguous), both given
+ *                   when rope_dim > 0; rope_dim in {0, 32, 64, 96, 128}.
+ *                   Channels c < rope_dim of Q and K (after the norm) become
+ *                   bf16(bf16(x[c] cos[s,c]) + bf16(rot[c] sin[s,c])) with
+ *                   rot[c] = -x[c + rope_dim/2] for c < rope_dim/2 and
+ *                   x[c - rope_dim/2] otherwise; other channels pass through.
+ *   S_pad      : padded length, a multiple of 128 and >= S
+ *   outputs (caller-allocated device memory, every byte written, padding zero):
+ *     q_i8, k_i8 : int8 [B, H, S_pad, 128], code = clamp(rint(x * (127/a)), -127, 127)
+ *                  with a = max |x| over the valid rows of the 32-row block
+ *     q_scale    : float [B, H, S_pad/32], (a/127) * c   (0 for an all-zero or padding block)
+ *     k_scale    : float [B, H, S_pad/32], a/127
+ *     v_fp8      : e4m3 bytes [B, H, 128, S_pad], code = e4m3_rn_satfinite(v * (448/a_ch)),
+ *                  a_ch = max over s < S of |v[b, s, h, ch]|
+ *     v_scale    : float [B, H, 128], a_ch / 448
+ *   workspace  : device scratch of at least sage_prepare_workspace_size(B, H)
+ *                bytes, 16-byte aligned; its contents on entry do not matter.
+ * Every binary32 operation above is rounded once to nearest-even (no fused
+ * multiply-add), so the outputs are a deterministic function of the inputs.
+ * Enqueues a memset and two kernels on `stream`.
+ */
+ATTN_API attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                         const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                         float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                         const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
+                         int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
+                         void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * sage_attn_workspace_size -- bytes of device scratch sage_attn_fwd needs:
+ * the INT8 Q and K codes widened to FP16, 2 * 2 * B * H * S_pad * 128 bytes.
+ * (sm_103a has no INT8 tensor-core MMA; the codes are widened exactly and the
+ * Q K^T product runs on the FP16 MMA, which is exact for these integers.)
+ */
+ATTN_API size_t sage_attn_workspace_size(int B, int H, int64_t S_pad);
+
+/*
+ * sage_attn_fwd -- attention on prepared tensors (layouts as sage_prepare writes them):
+ *   t[r, j] = (q_i8[r] . k_i8[j]) * q_scale[r/32] * k_scale[j/32]   (exact integer dot
+ *             product; Q's scale carries softmax_scale * log2 e, so t is in log2 units),
+ *             keys j >= S are masked out;
+ *   O[r, d] = v_scale[d] * sum_j e4m3(p'[r,j]) v_fp8[d, j] / sum_j p'[r,j],
+ *             p'[r,j] = 448 * 2^-4 * 2^(t[r,j] - m_r), m_r a running row maximum that
+ *             is raised whenever a tile's maximum exceeds it by more than 4; the
+ *             constant cancels in the ratio.  FP32 accumulation, one BF16 rounding.
+ *   o          : BF16 [B, S, H, 128] output with element strides o_str.
+ *   workspace  : device scratch of at least sage_attn_workspace_size(B, H, S_pad) bytes,
+ *                16-byte aligned; overwritten, contents on entry do not matter.
+ * Enqueues two kernels on `stream`.
+ */
+ATTN_API attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t* v_fp8, const float* q_scale,
+                          const float* k_scale, const float* v_scale, void* o, const int64_t o_str[3], int B,
+                          int S, int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then read and clear the
+ * device error words of all kernels.  ATTN_OK if no bounded wait ran out
+ * since the last call, ATTN_ERR_DEVICE_TIMEOUT otherwise, ATTN_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+ATTN_API attn_status attn_get_device_status(attn_stream_t stream);
+
+/* attn_last_error -- message of the calling thread's last failed call ("" if none). */
+ATTN_API const char* attn_last_error(void);
+
+/* attn_status_name -- the enumerator's name, e.g. "ATTN_ERR_ALIGNMENT". */
+ATTN_API const char* attn_status_name(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGEATTN_H_ */

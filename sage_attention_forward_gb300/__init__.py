@@ -1,0 +1,206 @@
+"""GB300 (sm_103a) attention forward: BF16 flash attention and the Sage
+INT8/FP8 variant, behind the C ABI declared in include/sageattn.h.
+
+This module only marshals torch tensors into the C calls of
+_build/libsageattn.so (pointers, shapes, strides, the current CUDA stream);
+every step of the computation runs in the library's CUDA kernels.  Output and
+scratch buffers the caller does not pass are allocated with torch.  If the
+library has not been built, every call raises.
+
+    attn_fwd_bf16(q, k, v)            -> O                 (BF16 [B, S, H, 128])
+    sage_prepare(q, k, v, ...)        -> Prepared           (INT8 Q/K, e4m3 V, scales)
+    sage_attn_fwd(prepared, S)        -> O
+    sage_attention(q, k, v, ...)      -> O                 (prepare + fwd)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+__all__ = ["AttnError", "attn_fwd_bf16", "sage_prepare", "sage_attn_fwd", "sage_attention", "Prepared",
+           "sage_padded_len", "attn_get_device_status", "lib", "STATUS"]
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_ALIGNMENT", 3: "ATTN_ERR_UNSUPPORTED",
+          4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_DEVICE_TIMEOUT"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+_lib = None
+_I64x3 = ctypes.c_int64 * 3
+_vp = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"CUDA library not built ({_LIB_PATH} missing): run `python -c 'import "
+                               f"__graft_entry__ as g; g.build()'` first")
+        L = ctypes.CDLL(_LIB_PATH)
+        i = ctypes.c_int
+        L.attn_fwd_bf16.argtypes = [_vp, _vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp]
+        L.attn_fwd_bf16.restype = i
+        L.sage_padded_len.argtypes = [ctypes.c_int64]
+        L.sage_padded_len.restype = ctypes.c_int64
+        L.sage_prepare_workspace_size.argtypes = [i, i]
+        L.sage_prepare_workspace_size.restype = ctypes.c_size_t
+        L.sage_prepare.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp, _vp,
+                                   ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                   ctypes.c_size_t, _vp]
+        L.sage_prepare.restype = i
+        L.sage_attn_workspace_size.argtypes = [i, i, ctypes.c_int64]
+        L.sage_attn_workspace_size.restype = ctypes.c_size_t
+        L.sage_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _I64x3, i, i, i, i, ctypes.c_int64, _vp,
+                                    ctypes.c_size_t, _vp]
+        L.sage_attn_fwd.restype = i
+        L.attn_get_device_status.argtypes = [_vp]
+        L.attn_get_device_status.restype = i
+        L.attn_last_error.argtypes = []
+        L.attn_last_error.restype = ctypes.c_char_p
+        L.attn_status_name.argtypes = [i]
+        L.attn_status_name.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise AttnError(status, lib().attn_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bshd(name: str, t: torch.Tensor):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, S, H, D], got {tuple(t.shape)}")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have unit channel stride")
+    sb, ss, sh, _ = t.stride()
+    return _I64x3(sb, ss, sh)
+
+
+def sage_padded_len(S: int) -> int:
+    return int(lib().sage_padded_len(S))
+
+
+def attn_fwd_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None,
+                  softmax_scale: float | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(softmax_scale * Q K^T) V for BF16 [B, S, H, 128] (any 16-byte-multiple strides)."""
+    B, S, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q.device)
+    qs, ks, vs, os_ = _bshd("q", q), _bshd("k", k), _bshd("v", v), _bshd("out", out)
+    _check(lib().attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, S, H, D, qs, ks, vs,
+                               os_, float(softmax_scale), _stream_ptr(stream)))
+    return out
+
+
+@dataclass
+class Prepared:
+    """Outputs of sage_prepare (device tensors, layouts of include/sageattn.h)."""
+    q_i8: torch.Tensor      # int8  [B, H, S_pad, 128]
+    k_i8: torch.Tensor      # int8  [B, H, S_pad, 128]
+    v_fp8: torch.Tensor     # uint8 [B, H, 128, S_pad] (e4m3 bit patterns)
+    q_scale: torch.Tensor   # fp32  [B, H, S_pad / 32]
+    k_scale: torch.Tensor   # fp32  [B, H, S_pad / 32]
+    v_scale: torch.Tensor   # fp32  [B, H, 128]
+    S: int
+    S_pad: int
+
+    @staticmethod
+    def empty(B: int, H: int, S: int, S_pad: int, device) -> "Prepared":
+        return Prepared(torch.empty((B, H, S_pad, 128), dtype=torch.int8, device=device),
+                        torch.empty((B, H, S_pad, 128), dtype=torch.int8, device=device),
+                        torch.empty((B, H, 128, S_pad), dtype=torch.uint8, device=device),
+                        torch.empty((B, H, S_pad // 32), dtype=torch.float32, device=device),
+                        torch.empty((B, H, S_pad // 32), dtype=torch.float32, device=device),
+                        torch.empty((B, H, 128), dtype=torch.float32, device=device), S, S_pad)
+
+
+def prepare_workspace(B: int, H: int, device) -> torch.Tensor:
+    return torch.empty(int(lib().sage_prepare_workspace_size(B, H)), dtype=torch.uint8, device=device)
+
+
+def attn_workspace(B: int, H: int, S_pad: int, device) -> torch.Tensor:
+    return torch.empty(int(lib().sage_attn_workspace_size(B, H, S_pad)), dtype=torch.uint8, device=device)
+
+
+def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: float | None = None,
+                 S_pad: int | None = None, q_norm_w: torch.Tensor | None = None,
+                 k_norm_w: torch.Tensor | None = None, rms_eps: float = 1e-6, rope_cos: torch.Tensor | None = None,
+                 rope_sin: torch.Tensor | None = None, rope_dim: int = 0, out: Prepared | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> Prepared:
+    """Quantise Q/K to INT8 and V to e4m3 (optionally RMSNorm + RoPE on Q/K first)."""
+    B, S, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if S_pad is None:
+        S_pad = sage_padded_len(S)
+    if out is None:
+        out = Prepared.empty(B, H, S, S_pad, q.device)
+    if workspace is None:
+        workspace = prepare_workspace(B, H, q.device)
+    qs, ks, vs = _bshd("q", q), _bshd("k", k), _bshd("v", v)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    _check(lib().sage_prepare(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
+                              float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
+                              ptr(rope_sin), int(rope_dim), int(S_pad), out.q_i8.data_ptr(), out.k_i8.data_ptr(),
+                              out.v_fp8.data_ptr(), out.q_scale.data_ptr(), out.k_scale.data_ptr(),
+                              out.v_scale.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+    return out
+
+
+def sage_attn_fwd(prep: Prepared, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Attention on prepared tensors -> BF16 [B, S, H, 128]."""
+    B, H, S_pad, D = prep.q_i8.shape
+    S = prep.S
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=prep.q_i8.device)
+    if workspace is None:
+        workspace = attn_workspace(B, H, S_pad, prep.q_i8.device)
+    os_ = _bshd("out", out)
+    _check(lib().sage_attn_fwd(prep.q_i8.data_ptr(), prep.k_i8.data_ptr(), prep.v_fp8.data_ptr(),
+                               prep.q_scale.data_ptr(), prep.k_scale.data_ptr(), prep.v_scale.data_ptr(),
+                               out.data_ptr(), os_, B, S, H, D, int(S_pad), workspace.data_ptr(), workspace.numel(),
+                               _stream_ptr(stream)))
+    return out
+
+
+def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
+                   rope_sin=None, rope_dim=0, out=None, stream=None) -> torch.Tensor:
+    """Prepare + attention: the SageAttention-style forward of BF16 Q/K/V."""
+    prep = sage_prepare(q, k, v, softmax_scale, None, q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim,
+                        stream=stream)
+    return sage_attn_fwd(prep, out=out, stream=stream)
+
+
+def attn_get_device_status(stream=None) -> None:
+    """Synchronise the stream and raise AttnError if a kernel gave up on a bounded wait."""
+    _check(lib().attn_get_device_status(_stream_ptr(stream)))

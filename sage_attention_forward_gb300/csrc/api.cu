@@ -1,0 +1,349 @@
+// C ABI of the library (declared in include/sageattn.h): argument validation,
+// TMA tensor-map encoding and kernel launches.  No allocation happens here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sageattn.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+attn_status fail(attn_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+attn_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr double kLog2e = 1.4426950408889634;
+
+// ------------------------------------------------------------------ device check
+constexpr int kMaxDevices = 64;
+int g_dev_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+std::mutex g_dev_mu;
+
+attn_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    if (g_dev_ok[dev] < 0) {
+      g_dev_ok[dev] = -1;
+      return fail(ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    }
+  }
+  if (g_dev_ok[dev] < 0) return fail(ATTN_ERR_UNSUPPORTED, "device %d is not an sm_103 device", dev);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+attn_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return ATTN_OK;
+}
+
+// BF16 [B, S, H, 128] with element strides (b, s, h): a 4-D map (d, s, h, b),
+// box 64 channels (128 bytes, 128-byte swizzle) x 128 rows.  Rows past S read as zero.
+attn_status tmap_bhsd_bf16(CUtensorMap* m, const void* ptr, int B, int S, int H, const long long str[3]) {
+  cuuint64_t dims[4] = {128, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)str[1] * 2, (cuuint64_t)str[2] * 2, (cuuint64_t)str[0] * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (BF16 [B,S,H,128]) failed: %d", (int)r);
+  return ATTN_OK;
+}
+
+// FP16 tensor [n2, n1, 128] (contiguous): a 3-D map with a 64 x 128 element
+// box (128 bytes wide, 128-byte swizzle).
+attn_status tmap_f16_rows(CUtensorMap* m, const void* ptr, long long n1, long long n2) {
+  cuuint64_t dims[3] = {128, (cuuint64_t)n1, (cuuint64_t)n2};
+  cuuint64_t strides[2] = {256, (cuuint64_t)(256 * n1)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (FP16 rows) failed: %d", (int)r);
+  return ATTN_OK;
+}
+
+// Byte tensor [n2, n1, n0] (contiguous rows of n0 bytes): a 3-D map with a
+// 128 x 128 byte box, 128-byte swizzle.
+attn_status tmap_bytes_3d(CUtensorMap* m, const void* ptr, long long n0, long long n1, long long n2) {
+  cuuint64_t dims[3] = {(cuuint64_t)n0, (cuuint64_t)n1, (cuuint64_t)n2};
+  cuuint64_t strides[2] = {(cuuint64_t)n0, (cuuint64_t)(n0 * n1)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (bytes) failed: %d", (int)r);
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_shape(int B, int S, int H, int D) {
+  if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dimension D=%d; only D=128 is supported", D);
+  if (B < 1 || S < 1 || H < 1) return fail(ATTN_ERR_INVALID_ARG, "B=%d S=%d H=%d must all be >= 1", B, S, H);
+  if (B > 65535 || H > 65535 || (long long)B * H > 65535)
+    return fail(ATTN_ERR_INVALID_ARG, "B=%d H=%d: B*H must be <= 65535", B, H);
+  return ATTN_OK;
+}
+
+// Strides of a [B, S, H, 128] tensor; a dimension of extent 1 gets a harmless
+// stand-in stride (never used to form an address).
+attn_status check_strides(const char* name, const void* ptr, const int64_t* in, int B, int S, int H,
+                          long long out[3]) {
+  if (ptr == nullptr) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(ptr)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+  if (in == nullptr) return fail(ATTN_ERR_INVALID_ARG, "%s strides are NULL", name);
+  const int ext[3] = {B, S, H};
+  const char* dn[3] = {"batch", "sequence", "head"};
+  for (int i = 0; i < 3; ++i) {
+    long long s = in[i];
+    if (ext[i] == 1) s = 128;
+    if (s <= 0) return fail(ATTN_ERR_INVALID_ARG, "%s %s stride %lld must be positive", name, dn[i], (long long)in[i]);
+    if (s % 8 != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "%s %s stride %lld is not a multiple of 8 elements", name, dn[i], s);
+    if (s >= (1ll << 38)) return fail(ATTN_ERR_INVALID_ARG, "%s %s stride %lld too large", name, dn[i], s);
+    out[i] = s;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+namespace sa {
+int device_sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+}  // namespace sa
+
+namespace {
+
+#define TRY(x)                          \
+  do {                                  \
+    attn_status _s = (x);               \
+    if (_s != ATTN_OK) return _s;       \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int H, int D,
+                          const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                          const int64_t o_str[3], float softmax_scale, attn_stream_t stream) {
+  TRY(check_shape(B, S, H, D));
+  long long qs[3], ks[3], vs[3], os[3];
+  TRY(check_strides("q", q, q_str, B, S, H, qs));
+  TRY(check_strides("k", k, k_str, B, S, H, ks));
+  TRY(check_strides("v", v, v_str, B, S, H, vs));
+  TRY(check_strides("o", o, o_str, B, S, H, os));
+  if (!std::isfinite(softmax_scale)) return fail(ATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
+  TRY(check_device());
+  TRY(get_encoder());
+  CUtensorMap tq, tk, tv;
+  TRY(tmap_bhsd_bf16(&tq, q, B, S, H, qs));
+  TRY(tmap_bhsd_bf16(&tk, k, B, S, H, ks));
+  TRY(tmap_bhsd_bf16(&tv, v, B, S, H, vs));
+  const float c = (float)((double)softmax_scale * kLog2e);
+  cudaError_t e = sa::launch_attn_bf16(tq, tk, tv, o, os[0], os[1], os[2], B, S, H, c, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_fwd_bf16 launch");
+  return ATTN_OK;
+}
+
+int64_t sage_padded_len(int64_t S) { return S <= 0 ? 0 : ((S + 127) / 128) * 128; }
+
+size_t sage_prepare_workspace_size(int B, int H) {
+  if (B < 1 || H < 1) return 0;
+  return (size_t)B * (size_t)H * 128 * sizeof(uint32_t);
+}
+
+attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                         const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                         float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                         const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
+                         int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
+                         void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  TRY(check_shape(B, S, H, D));
+  sa::PrepareArgs a;
+  TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
+  TRY(check_strides("k", k, k_str, B, S, H, a.str[1]));
+  TRY(check_strides("v", v, v_str, B, S, H, a.str[2]));
+  if (!std::isfinite(softmax_scale)) return fail(ATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (S_pad < S || S_pad % 128 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
+  if (S_pad / 32 > (1ll << 30)) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
+  if (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w)))
+    return fail(ATTN_ERR_ALIGNMENT, "RMSNorm weights must be 16-byte aligned");
+  if (q_norm_w && !(rms_eps >= 0.0f && std::isfinite(rms_eps)))
+    return fail(ATTN_ERR_INVALID_ARG, "rms_eps must be finite and >= 0");
+  if (!(rope_dim == 0 || rope_dim == 32 || rope_dim == 64 || rope_dim == 96 || rope_dim == 128))
+    return fail(ATTN_ERR_INVALID_ARG, "rope_dim=%d must be one of 0, 32, 64, 96, 128", rope_dim);
+  if (rope_dim > 0) {
+    if (!rope_cos || !rope_sin) return fail(ATTN_ERR_INVALID_ARG, "rope_dim > 0 needs rope_cos and rope_sin");
+    if (!aligned16(rope_cos) || !aligned16(rope_sin))
+      return fail(ATTN_ERR_ALIGNMENT, "RoPE tables must be 16-byte aligned");
+  }
+  struct {
+    const char* n;
+    const void* p;
+  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale},
+              {"k_scale", k_scale}, {"v_scale", v_scale}, {"workspace", workspace}};
+  for (auto& t : outs) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  if (workspace_bytes < sage_prepare_workspace_size(B, H))
+    return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
+                sage_prepare_workspace_size(B, H));
+  TRY(check_device());
+  a.x[0] = q;
+  a.x[1] = k;
+  a.x[2] = v;
+  a.B = B;
+  a.S = S;
+  a.H = H;
+  a.S_pad = S_pad;
+  a.q_norm_w = q_norm_w;
+  a.k_norm_w = k_norm_w;
+  a.rms_eps = rms_eps;
+  a.rope_cos = rope_dim > 0 ? rope_cos : nullptr;
+  a.rope_sin = rope_dim > 0 ? rope_sin : nullptr;
+  a.rope_dim = rope_dim;
+  a.q_i8 = q_i8;
+  a.k_i8 = k_i8;
+  a.v_fp8 = v_fp8;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.c_log2 = (float)((double)softmax_scale * kLog2e);
+  a.vmax = reinterpret_cast<uint32_t*>(workspace);
+  cudaError_t e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare launch");
+  return ATTN_OK;
+}
+
+size_t sage_attn_workspace_size(int B, int H, int64_t S_pad) {
+  if (B < 1 || H < 1 || S_pad < 1) return 0;
+  return (size_t)4 * (size_t)B * (size_t)H * (size_t)S_pad * 128;
+}
+
+attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t* v_fp8, const float* q_scale,
+                          const float* k_scale, const float* v_scale, void* o, const int64_t o_str[3], int B,
+                          int S, int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream) {
+  TRY(check_shape(B, S, H, D));
+  if (S_pad < S || S_pad % 128 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
+  if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  struct {
+    const char* n;
+    const void* p;
+  } ins[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale}, {"k_scale", k_scale},
+             {"v_scale", v_scale}, {"workspace", workspace}};
+  for (auto& t : ins) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  if (workspace_bytes < sage_attn_workspace_size(B, H, S_pad))
+    return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
+                sage_attn_workspace_size(B, H, S_pad));
+  long long os[3];
+  TRY(check_strides("o", o, o_str, B, S, H, os));
+  TRY(check_device());
+  TRY(get_encoder());
+  const long long bh = (long long)B * H;
+  const long long n_codes = bh * S_pad * 128;
+  uint8_t* q16 = reinterpret_cast<uint8_t*>(workspace);
+  uint8_t* k16 = q16 + 2 * n_codes;
+  CUtensorMap tq, tk, tv;
+  TRY(tmap_f16_rows(&tq, q16, S_pad, bh));
+  TRY(tmap_f16_rows(&tk, k16, S_pad, bh));
+  TRY(tmap_bytes_3d(&tv, v_fp8, S_pad, 128, bh));
+  cudaError_t e = sa::launch_sage_widen(q_i8, k_i8, q16, k16, n_codes, sa::device_sm_count(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd widen launch");
+  e = sa::launch_sage_attn(tq, tk, tv, q_scale, k_scale, v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd launch");
+  return ATTN_OK;
+}
+
+attn_status attn_get_device_status(attn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  uint32_t w1 = 0, w2 = 0;
+  e = sa::read_and_clear_err_bf16(&w1);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
+  e = sa::read_and_clear_err_sage(&w2);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
+  if (w1 | w2)
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (attn_fwd_bf16 bits 0x%x, sage_attn_fwd bits 0x%x)",
+                w1, w2);
+  return ATTN_OK;
+}
+
+const char* attn_last_error(void) { return g_msg; }
+
+const char* attn_status_name(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+  }
+  return "ATTN_UNKNOWN_STATUS";
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// Host-side launchers of the device kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace sa {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// BF16 flash attention (attn_bf16.cu)
+size_t attn_bf16_smem_bytes();
+cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
+                             long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
+                             cudaStream_t stream);
+cudaError_t read_and_clear_err_bf16(uint32_t* out);
+
+// Sage prepare (sage_prepare.cu)
+struct PrepareArgs {
+  const void* x[3];          // q, k, v (BF16)
+  long long str[3][3];       // element strides (b, s, h)
+  int B, S, H;
+  long long S_pad;
+  const void* q_norm_w;
+  const void* k_norm_w;
+  float rms_eps;
+  const void* rope_cos;
+  const void* rope_sin;
+  int rope_dim;
+  int8_t* q_i8;
+  int8_t* k_i8;
+  uint8_t* v_fp8;
+  float* q_scale;
+  float* k_scale;
+  float* v_scale;
+  float c_log2;
+  uint32_t* vmax;            // workspace: B*H*128 words
+};
+cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
+
+// Sage attention on prepared tensors (sage_attn.cu)
+size_t sage_attn_smem_bytes();
+cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,
+                              int num_sms, cudaStream_t stream);
+cudaError_t launch_sage_attn(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, const CUtensorMap& tm_v8,
+                             const float* q_scale, const float* k_scale, const float* v_scale, void* o,
+                             long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
+                             cudaStream_t stream);
+cudaError_t read_and_clear_err_sage(uint32_t* out);
+
+}  // namespace sa

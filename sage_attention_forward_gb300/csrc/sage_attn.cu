@@ -1,0 +1,460 @@
+// SageAttention-style forward on prepared tensors, for sm_103a.
+//
+// What it computes (aiter pull request "gfx1201_sage_prepare /
+// gfx1201_sage_attention", commit message of gfx1201_sage_attention;
+// Technical Details): Q K^T on the INT8 codes, online softmax in base 2 (Q's
+// scale already carries softmax_scale * log2(e)), P V with P and V in FP8
+// e4m3, FP32 accumulation, BF16 output:
+//   t[r, j] = (q_i8[r] . k_i8[j]) * q_scale[r / 32] * k_scale[j / 32]
+//   O[r, d] = v_scale[d] * sum_j e4m3(p'[r, j]) v_fp8[d, j] / sum_j p'[r, j]
+//   p'[r, j] = 448 * 2^-kTau * 2^(t[r, j] - m_r)
+// where m_r is the row's reference maximum (see below); the constant factor
+// 448 * 2^-kTau keeps p' inside the e4m3 range and cancels in the ratio.
+//
+// sm_103a has no INT8 tensor-core MMA (tcgen05 kind::i8 is not accepted for
+// this target), so the codes are widened to FP16 -- exactly, |code| <= 127 --
+// by a streaming pass into the caller's workspace, and Q K^T runs on
+// tcgen05 kind::f16 with an FP32 accumulator.  That product is exact: every
+// partial sum is an integer of magnitude <= 128 * 127^2 < 2^24.  P V runs on
+// tcgen05 kind::f8f6f4 with P (e4m3, four per TMEM column) taken from TMEM
+// and V^T from shared memory, where the [B, H, 128, S_pad] layout makes it the
+// K-major operand directly.
+//
+// Structure is that of the BF16 kernel: one CTA = (batch, head, two 128-row
+// Q tiles), 320 threads; warp 8 TMA producer (Q once, then K_j into a 3-slot
+// ring of FP16 tiles and V_j into a 3-slot ring of e4m3 tiles), warp 9 MMA
+// issuer, warps 0-3 and 4-7 one softmax thread per row for Q tile 0 and 1.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P_i
+// (e4m3) overwrites the first 32 columns of S_i.  The reference maximum moves
+// only when a tile's maximum exceeds it by more than kTau (log2 units).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kNQ = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kQTileBytes = 128 * 128 * 2;   // FP16 128 x 128
+constexpr int kHalfBytes = kQTileBytes / 2;  // [128 rows][64 columns] FP16 sub-tile
+constexpr int kVTileBytes = 128 * 128;       // e4m3 [128 d][128 positions]
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr float kTau = 4.0f;
+constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
+
+struct __align__(1024) Smem {
+  uint8_t q[kNQ][kQTileBytes];
+  uint8_t k[kKStages][kQTileBytes];
+  uint8_t v[kVStages][kVTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[kNQ];
+  uint64_t p_full[kNQ];
+  uint64_t o_done[kNQ];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+__device__ uint32_t g_err_sage;
+
+struct Params {
+  const float* q_scale;   // [B*H, nblk]
+  const float* k_scale;   // [B*H, nblk]
+  const float* v_scale;   // [B*H, 128]
+  __nv_bfloat16* o;
+  long long o_sb, o_ss, o_sh;
+  int S;
+  int H;
+  int nblk;               // S_pad / 32
+  int n_tiles;            // ceil(S / 128)
+};
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int q_row0 = blockIdx.x * (kNQ * kBM);
+  const int n = p.n_tiles;
+  volatile uint32_t* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int i = 0; i < kNQ; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.o_done[i], 1);
+    }
+    mbar_init(&sm.mma_drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kWarpLoad) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&sm.q_full, kNQ * kQTileBytes);
+      for (int i = 0; i < kNQ; ++i)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        {
+          const int slot = j % kKStages, use = j / kKStages;
+          if (use > 0 && !mbar_wait(&sm.k_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.k_full[slot], kQTileBytes);
+          tma_load_3d(sm.k[slot], &tm_k, &sm.k_full[slot], 0, j * kBN, bh);
+          tma_load_3d(sm.k[slot] + kHalfBytes, &tm_k, &sm.k_full[slot], 64, j * kBN, bh);
+          k_issued = j + 1;
+        }
+        {
+          const int slot = j % kVStages, use = j / kVStages;
+          if (use > 0 && !mbar_wait(&sm.v_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.v_full[slot], kVTileBytes);
+          tma_load_3d(sm.v[slot], &tm_v, &sm.v_full[slot], j * kBN, 0, bh);
+          v_issued = j + 1;
+        }
+      }
+      if (*abort_flag) {
+        mbar_wait_teardown(&sm.q_full, 0);
+        for (int it = (k_issued > kKStages ? k_issued - kKStages : 0); it < k_issued; ++it)
+          mbar_wait_teardown(&sm.k_full[it % kKStages], (it / kKStages) & 1);
+        for (int it = (v_issued > kVStages ? v_issued - kVStages : 0); it < v_issued; ++it)
+          mbar_wait_teardown(&sm.v_full[it % kVStages], (it / kVStages) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc_qk = idesc_f32acc(kFmtF16, kFmtF16, false, false, kBM, kBN);
+      const uint32_t idesc_pv = idesc_f32acc(kFmtE4M3, kFmtE4M3, false, false, kBM, 128);
+      // TMEM columns of S_i and O_i
+      auto tS = [&](int i) { return tmem + 128u * (uint32_t)i; };
+      auto tO = [&](int i) { return tmem + 256u + 128u * (uint32_t)i; };
+      uint32_t* err = &g_err_sage;
+
+      auto issue_s = [&](int i, int slot) {
+        const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[slot]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_f16_ss(tS(i), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_qk,
+                     kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int slot, bool acc) {
+        const uint32_t va = smem_u32(sm.v[slot]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // 32 positions (bytes) per step inside the 128-byte swizzled rows of V^T
+          mma_f8_ts(tO(i), tS(i) + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), idesc_pv,
+                    (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = mbar_wait(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        mma_commit(&sm.s_full[0]);
+        issue_s(1, 0);
+        mma_commit(&sm.s_full[1]);
+        mma_commit(&sm.k_empty[0]);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int slotV = j % kVStages;
+        const int slotK = (j + 1) % kKStages;
+        const bool more = (j + 1 < n);
+        if (!mbar_wait(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+        if (!mbar_wait(&sm.p_full[0], j & 1, abort_flag, err, kErrTimeoutSync)) break;
+        tc_fence_after();
+        issue_pv(0, slotV, j > 0);
+        mma_commit(&sm.o_done[0]);
+        if (more) {
+          if (!mbar_wait(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+          tc_fence_after();
+          issue_s(0, slotK);
+          mma_commit(&sm.s_full[0]);
+        }
+        if (!mbar_wait(&sm.p_full[1], j & 1, abort_flag, err, kErrTimeoutSync)) break;
+        tc_fence_after();
+        issue_pv(1, slotV, j > 0);
+        mma_commit(&sm.o_done[1]);
+        mma_commit(&sm.v_empty[slotV]);
+        if (more) {
+          issue_s(1, slotK);
+          mma_commit(&sm.s_full[1]);
+          mma_commit(&sm.k_empty[slotK]);
+        }
+      }
+      mma_commit(&sm.mma_drain);
+      mbar_wait_teardown(&sm.mma_drain, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int i = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128u * i;
+    const uint32_t tO = tmem + lane_off + 256u + 128u * i;
+    const int grow = q_row0 + i * kBM + row;
+    // row's Q scale (carries softmax_scale * log2 e); rows past S use block 0's slot of a real block
+    const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
+    const float qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
+    const float* ksp = p.k_scale + (long long)bh * p.nblk;
+    uint32_t* err = &g_err_sage;
+    float m_used = -INFINITY, l = 0.0f;
+    bool ok = true;
+    float4 ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
+
+    for (int j = 0; j < n; ++j) {
+      const float4 ks4 = ks_next;
+      if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
+      const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
+      if (!mbar_wait_warp(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_ld_wait();
+      // keys past S: excluded from the maximum here and given probability 0 below
+      // (their scale may be 0, and 0 * -inf would be NaN)
+      const int valid = p.S - j * kBN;
+      if (valid < kBN) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (e >= valid) s[e] = f2u(-INFINITY);
+      }
+      float m_cand = -INFINITY;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float mx = fmax3(u2f(s[32 * blk]), u2f(s[32 * blk + 1]), u2f(s[32 * blk + 2]));
+#pragma unroll
+        for (int e = 3; e < 31; e += 2) mx = fmax3(mx, u2f(s[32 * blk + e]), u2f(s[32 * blk + e + 1]));
+        mx = fmaxf(mx, u2f(s[32 * blk + 31]));
+        // scales are >= 0, so the block's largest t is f * (largest raw score); a block
+        // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
+        m_cand = fmaxf(m_cand, mx * f[blk]);
+      }
+      const bool need = m_cand > m_used + kTau;
+      // a row whose tile maximum passed its reference by more than kTau moves the
+      // reference; O and l are brought to the new reference by the factor sc
+      const float sc = need ? ex2_approx(m_used - m_cand) : 1.0f;
+      if (need) {
+        l *= sc;
+        m_used = m_cand;
+      }
+      const float off = m_used + kTau - kLog2_448;
+      float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        // 32 scores of key block blk -> 8 words of four e4m3 each, P columns [8blk, 8blk + 8)
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float p0 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 0]), f[blk], -off));
+          float p1 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 1]), f[blk], -off));
+          float p2 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 2]), f[blk], -off));
+          float p3 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 3]), f[blk], -off));
+          if (valid < kBN) {
+            const int c0 = 32 * blk + 4 * e;
+            p0 = c0 + 0 < valid ? p0 : 0.0f;
+            p1 = c0 + 1 < valid ? p1 : 0.0f;
+            p2 = c0 + 2 < valid ? p2 : 0.0f;
+            p3 = c0 + 3 < valid ? p3 : 0.0f;
+          }
+          rs0 += p0 + p1;
+          rs1 += p2 + p3;
+          pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+        tmem_st8(tS + 8 * blk, pk);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O_i must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already stored)
+        if (!mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+          tmem_st_wait();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * cc, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * sc);
+          tmem_st32(tO + 32 * cc, o);
+        }
+      }
+      tmem_st_wait();
+      l += rs0 + rs1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[i]);
+    }
+
+    if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const float* vs = p.v_scale + (long long)bh * 128;
+      const int b = bh / p.H, h = bh % p.H;
+      __nv_bfloat16* dst = p.o + (long long)b * p.o_sb + (long long)grow * p.o_ss + (long long)h * p.o_sh;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * cc, o);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 sv = __ldg(reinterpret_cast<const float2*>(vs + 32 * cc + 2 * e));
+          w[e] = pack_bf16x2(u2f(o[2 * e]) * (sv.x * inv_l), u2f(o[2 * e + 1]) * (sv.y * inv_l));
+        }
+        if (grow < p.S) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// INT8 codes -> FP16, exactly: 16 codes per thread and iteration.  For a byte
+// u = code + 128, the FP16 pattern 0x6400 | u is 1024 + u, so subtracting 1152
+// gives the code.
+__global__ void __launch_bounds__(256) widen_i8_f16_kernel(const int8_t* __restrict__ q8, const int8_t* __restrict__ k8,
+                                                          __half* __restrict__ q16, __half* __restrict__ k16,
+                                                          long long n16) {
+  const int8_t* src = blockIdx.y == 0 ? q8 : k8;
+  __half* dst = blockIdx.y == 0 ? q16 : k16;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152, 1152
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    const uint32_t in[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    uint32_t out[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint32_t lo = __byte_perm(in[t], 0x64646464u, 0x5140);
+      uint32_t hi = __byte_perm(in[t], 0x64646464u, 0x7362);
+      __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+      __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+      out[2 * t] = *reinterpret_cast<uint32_t*>(&hl);
+      out[2 * t + 1] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+    d[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+}  // namespace
+
+size_t sage_attn_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,
+                              int num_sms, cudaStream_t stream) {
+  const long long n16 = n_codes / 16;
+  long long blocks = (n16 + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  dim3 grid((unsigned)blocks, 2, 1);
+  widen_i8_f16_kernel<<<grid, 256, 0, stream>>>(q8, k8, reinterpret_cast<__half*>(q16), reinterpret_cast<__half*>(k16),
+                                                n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sage_attn(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, const CUtensorMap& tm_v8,
+                             const float* q_scale, const float* k_scale, const float* v_scale, void* o,
+                             long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
+                             cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  const size_t smem = sage_attn_smem_bytes();
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  Params p;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.o_sb = o_sb;
+  p.o_ss = o_ss;
+  p.o_sh = o_sh;
+  p.S = S;
+  p.H = H;
+  p.nblk = (int)(S_pad / 32);
+  p.n_tiles = (S + kBN - 1) / kBN;
+  dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
+  sage_attn_kernel<<<grid, kThreads, smem, stream>>>(tm_q16, tm_k16, tm_v8, p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_err_sage(uint32_t* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_err_sage, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  return cudaMemcpyToSymbol(g_err_sage, &zero, sizeof(uint32_t));
+}
+
+}  // namespace sa

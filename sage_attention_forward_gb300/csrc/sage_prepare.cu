@@ -1,0 +1,360 @@
+// Sage prepare for sm_103a: BF16 Q/K -> INT8 (per 32-row block scale), BF16 V ->
+// FP8 e4m3 transposed (per channel scale), with optional QK RMSNorm and
+// rotate-half RoPE first.  Follows the aiter pull request "gfx1201_sage_prepare
+// / gfx1201_sage_attention" (commit message of gfx1201_sage_prepare; Technical
+// Details).  Every binary32 operation uses an explicitly rounded intrinsic
+// (no contraction), so the bytes written are a deterministic function of the
+// inputs, and the order of the one order-dependent sum (RMSNorm's sum of
+// squares) is fixed below.
+//
+// Kernel 1 (grid.z = 0: Q, 1: K, 2: V maxima) -- one warp per (b, h, 32-row
+// block).  A row of 128 channels is held by 8 lanes, lane L of the group owning
+// channels [16L, 16L + 16) (two 128-bit loads); a warp covers 4 rows per step
+// and 32 rows in 8 steps, so every lane keeps 8 rows x 16 channels in
+// registers while the block maximum is reduced.  For V the same warps only
+// take per-channel maxima, reduce them across the CTA and fold them into the
+// workspace with integer atomicMax on the (non-negative) float bits.
+// Kernel 2 -- one CTA per (b, h, 128 positions): 128 threads, thread (c8, sg)
+// loads 16 positions x 8 channels, encodes them and transposes the bytes in
+// registers (byte permutes) into 8 rows of 16 consecutive positions, which it
+// writes with 128-bit stores into the [B, H, 128, S_pad] layout.
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+struct QKParams {
+  const __nv_bfloat16* x[3];
+  long long sb[3], ss[3], sh[3];
+  int B, S, H;
+  long long S_pad;
+  int nblk;                         // S_pad / 32
+  const __nv_bfloat16* norm_w[2];   // Q, K (nullptr: no RMSNorm)
+  float eps;
+  const __nv_bfloat16* rope_cos;    // [S, rope_dim]
+  const __nv_bfloat16* rope_sin;
+  int rope_dim;
+  int8_t* codes[2];
+  float* scales[2];
+  float c_log2;                     // fl32(softmax_scale * log2 e), folded into Q's scales
+  uint32_t* vmax;                   // [B*H*128] float bits of the channel maxima of |V|
+};
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf_round(float f) {
+  return __bfloat162float(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&f)[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf_lo(w[i]);
+    f[2 * i + 1] = bf_hi(w[i]);
+  }
+}
+__device__ __forceinline__ void pack16(const float (&f)[16], uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = bf_pack(f[2 * i], f[2 * i + 1]);
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* src, uint32_t (&w)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+__global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
+  const int task = blockIdx.z;
+  const int bh = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x * 8 + warp;
+  const int g = lane >> 3;   // row inside a 4-row step
+  const int L = lane & 7;    // channel group [16L, 16L+16)
+  const __nv_bfloat16* base = p.x[task] + (long long)b * p.sb[task] + (long long)h * p.sh[task] + 16 * L;
+  const long long ss = p.ss[task];
+
+  if (task == 2) {
+    // -------------------------------------------------------- V channel maxima
+    __shared__ float red[8][128];
+    float mx[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) mx[k] = 0.0f;
+    if (blk < p.nblk) {
+#pragma unroll
+      for (int step = 0; step < 8; ++step) {
+        const int s = 32 * blk + 4 * step + g;
+        if (s < p.S) {
+          uint32_t w[8];
+          load16(base + (long long)s * ss, w);
+          float f[16];
+          unpack16(w, f);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], fabsf(f[k]));
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
+      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
+    }
+    if (g == 0) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) red[warp][16 * L + k] = mx[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      float m = red[0][threadIdx.x];
+#pragma unroll
+      for (int w2 = 1; w2 < 8; ++w2) m = fmaxf(m, red[w2][threadIdx.x]);
+      if (m > 0.0f) atomicMax(&p.vmax[(long long)bh * 128 + threadIdx.x], __float_as_uint(m));
+    }
+    return;
+  }
+
+  if (blk >= p.nblk) return;
+  // ---------------------------------------------------------- load 8 rows x 16 channels
+  uint32_t x[8][8];
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    const int s = 32 * blk + 4 * step + g;
+    if (s < p.S) {
+      load16(base + (long long)s * ss, x[step]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[step][i] = 0u;
+    }
+  }
+
+  // ---------------------------------------------------------- RMSNorm (optional)
+  const __nv_bfloat16* nw = p.norm_w[task];
+  if (nw != nullptr) {
+    uint32_t ww[8];
+    load16(nw + 16 * L, ww);
+    float wf[16];
+    unpack16(ww, wf);
+#pragma unroll
+    for (int step = 0; step < 8; ++step) {
+      float f[16];
+      unpack16(x[step], f);
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = __fadd_rn(acc, __fmul_rn(f[i], f[i]));
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
+      const float ms = __fmul_rn(acc, 1.0f / 128.0f);
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = bf_round(__fmul_rn(bf_round(__fmul_rn(f[i], r)), wf[i]));
+      pack16(f, x[step]);
+    }
+  }
+
+  // ---------------------------------------------------------- rotate-half RoPE (optional)
+  if (p.rope_dim > 0) {
+    const int hh = p.rope_dim >> 1;
+    const bool lo_half = 16 * L < hh;
+    const bool in_rope = 16 * L < p.rope_dim;
+    int src = lo_half ? L + (hh >> 4) : L - (hh >> 4);
+    if (!in_rope) src = L;
+    const int src_lane = (lane & ~7) | src;
+#pragma unroll
+    for (int step = 0; step < 8; ++step) {
+      uint32_t partner[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) partner[i] = __shfl_sync(0xffffffffu, x[step][i], src_lane);
+      const int s = 32 * blk + 4 * step + g;
+      if (in_rope && s < p.S) {
+        uint32_t cw[8], sw[8];
+        load16(p.rope_cos + (long long)s * p.rope_dim + 16 * L, cw);
+        load16(p.rope_sin + (long long)s * p.rope_dim + 16 * L, sw);
+        float f[16], pf[16], cf[16], sf[16];
+        unpack16(x[step], f);
+        unpack16(partner, pf);
+        unpack16(cw, cf);
+        unpack16(sw, sf);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float rot = lo_half ? -pf[i] : pf[i];
+          const float a = bf_round(__fmul_rn(f[i], cf[i]));
+          const float bb = bf_round(__fmul_rn(rot, sf[i]));
+          f[i] = bf_round(__fadd_rn(a, bb));
+        }
+        pack16(f, x[step]);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------- block maximum and INT8 codes
+  float a = 0.0f;
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    const int s = 32 * blk + 4 * step + g;
+    if (s < p.S) {
+      float f[16];
+      unpack16(x[step], f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+  const float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
+  int8_t* out = p.codes[task] + ((long long)bh * p.S_pad) * 128 + 16 * L;
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    const int s = 32 * blk + 4 * step + g;
+    uint32_t q[4] = {0u, 0u, 0u, 0u};
+    if (s < p.S) {
+      float f[16];
+      unpack16(x[step], f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        int v = __float2int_rn(__fmul_rn(f[i], inv));
+        v = max(-127, min(127, v));
+        q[i >> 2] |= (uint32_t)(v & 0xff) << (8 * (i & 3));
+      }
+    }
+    *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+  if (lane == 0) {
+    float sc = 0.0f;
+    if (a > 0.0f) {
+      sc = __fdiv_rn(a, 127.0f);
+      if (task == 0) sc = __fmul_rn(sc, p.c_log2);
+    }
+    p.scales[task][(long long)bh * p.nblk + blk] = sc;
+  }
+}
+
+struct VParams {
+  const __nv_bfloat16* v;
+  long long sb, ss, sh;
+  int B, S, H;
+  long long S_pad;
+  const uint32_t* vmax;
+  uint8_t* codes;   // [B, H, 128, S_pad]
+  float* scales;    // [B, H, 128]
+};
+
+// 4 words (rows r..r+3, each holding 4 channel bytes, channel 0 lowest) ->
+// 4 words (channels 0..3, each holding the 4 row bytes, row r lowest).
+__device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& o0,
+                                             uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  const uint32_t t0 = __byte_perm(a, b, 0x5140);  // a0 b0 a1 b1
+  const uint32_t t1 = __byte_perm(a, b, 0x7362);  // a2 b2 a3 b3
+  const uint32_t t2 = __byte_perm(c, d, 0x5140);  // c0 d0 c1 d1
+  const uint32_t t3 = __byte_perm(c, d, 0x7362);  // c2 d2 c3 d3
+  o0 = __byte_perm(t0, t2, 0x5410);               // a0 b0 c0 d0
+  o1 = __byte_perm(t0, t2, 0x7632);               // a1 b1 c1 d1
+  o2 = __byte_perm(t1, t3, 0x5410);
+  o3 = __byte_perm(t1, t3, 0x7632);
+}
+
+__global__ void __launch_bounds__(128) prep_v_kernel(const VParams p) {
+  const int bh = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
+  const int c8 = threadIdx.x & 15;        // channels [8*c8, 8*c8 + 8)
+  const int sg = threadIdx.x >> 4;        // positions [s0, s0 + 16)
+  const long long s0 = (long long)blockIdx.x * 128 + 16 * sg;
+
+  float inv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float a = __uint_as_float(p.vmax[(long long)bh * 128 + 8 * c8 + k]);
+    inv[k] = (a > 0.0f) ? __fdiv_rn(448.0f, a) : 0.0f;
+    if (blockIdx.x == 0 && sg == 0) p.scales[(long long)bh * 128 + 8 * c8 + k] = (a > 0.0f) ? __fdiv_rn(a, 448.0f) : 0.0f;
+  }
+
+  const __nv_bfloat16* base = p.v + (long long)b * p.sb + (long long)h * p.sh + 8 * c8;
+  uint32_t lo[16], hi[16];   // row r: channel bytes 0..3 and 4..7
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const long long s = s0 + r;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (s < p.S) w = __ldg(reinterpret_cast<const uint4*>(base + s * p.ss));
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __fmul_rn(bf_lo(wv[i]), inv[2 * i]);
+      f[2 * i + 1] = __fmul_rn(bf_hi(wv[i]), inv[2 * i + 1]);
+    }
+    lo[r] = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    hi[r] = pack_e4m3x4(f[4], f[5], f[6], f[7]);
+  }
+  uint32_t col[8][4];  // channel k, positions 4*t .. 4*t+3 in word t
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    transpose4x4(lo[4 * t], lo[4 * t + 1], lo[4 * t + 2], lo[4 * t + 3], col[0][t], col[1][t], col[2][t], col[3][t]);
+    transpose4x4(hi[4 * t], hi[4 * t + 1], hi[4 * t + 2], hi[4 * t + 3], col[4][t], col[5][t], col[6][t], col[7][t]);
+  }
+  uint8_t* out = p.codes + ((long long)bh * 128 + 8 * c8) * p.S_pad + s0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<uint4*>(out + (long long)k * p.S_pad) = make_uint4(col[k][0], col[k][1], col[k][2], col[k][3]);
+}
+
+}  // namespace
+
+cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
+  const int nblk = (int)(a.S_pad / 32);
+  cudaError_t e = cudaMemsetAsync(a.vmax, 0, (size_t)a.B * a.H * 128 * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  QKParams p;
+  for (int t = 0; t < 3; ++t) {
+    p.x[t] = reinterpret_cast<const __nv_bfloat16*>(a.x[t]);
+    p.sb[t] = a.str[t][0];
+    p.ss[t] = a.str[t][1];
+    p.sh[t] = a.str[t][2];
+  }
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.S_pad = a.S_pad;
+  p.nblk = nblk;
+  p.norm_w[0] = reinterpret_cast<const __nv_bfloat16*>(a.q_norm_w);
+  p.norm_w[1] = reinterpret_cast<const __nv_bfloat16*>(a.k_norm_w);
+  p.eps = a.rms_eps;
+  p.rope_cos = reinterpret_cast<const __nv_bfloat16*>(a.rope_cos);
+  p.rope_sin = reinterpret_cast<const __nv_bfloat16*>(a.rope_sin);
+  p.rope_dim = a.rope_dim;
+  p.codes[0] = a.q_i8;
+  p.codes[1] = a.k_i8;
+  p.scales[0] = a.q_scale;
+  p.scales[1] = a.k_scale;
+  p.c_log2 = a.c_log2;
+  p.vmax = a.vmax;
+  dim3 g1((nblk + 7) / 8, a.B * a.H, 3);
+  prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  VParams vp;
+  vp.v = reinterpret_cast<const __nv_bfloat16*>(a.x[2]);
+  vp.sb = a.str[2][0];
+  vp.ss = a.str[2][1];
+  vp.sh = a.str[2][2];
+  vp.B = a.B;
+  vp.S = a.S;
+  vp.H = a.H;
+  vp.S_pad = a.S_pad;
+  vp.vmax = a.vmax;
+  vp.codes = a.v_fp8;
+  vp.scales = a.v_scale;
+  dim3 g2((unsigned)(a.S_pad / 128), a.B * a.H, 1);
+  prep_v_kernel<<<g2, 128, 0, stream>>>(vp);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

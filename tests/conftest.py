@@ -20,3 +20,23 @@ def cuda_dev():
     if not torch.cuda.is_available():
         pytest.fail("gpu test needs CUDA, none is available")
     return torch.device("cuda:0")
+
+
+_INPUT_CACHE = {}
+
+
+@pytest.fixture(scope="session")
+def workload_inputs():
+    """Session cache: name -> (CPU Inputs, device Inputs) for the named workloads."""
+    import torch
+    from workloads import WORKLOADS, make_inputs, to_device
+
+    def get(name):
+        if name not in _INPUT_CACHE:
+            cpu = make_inputs(WORKLOADS[name])
+            dev = to_device(cpu, torch.device("cuda:0"))
+            _INPUT_CACHE[name] = (cpu, dev)
+        return _INPUT_CACHE[name]
+
+    yield get
+    _INPUT_CACHE.clear()

@@ -1,0 +1,102 @@
+"""The C ABI loads, exports what include/sageattn.h declares, and rejects bad
+arguments on the host before touching the GPU (CPU-only tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sage_attention_forward_gb300 as sa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sageattn.h")
+
+I64x3 = ctypes.c_int64 * 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"attn_fwd_bf16", "sage_prepare", "sage_attn_fwd"} <= set(names)
+    L = sa.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_names_and_padded_length():
+    L = sa.lib()
+    for code, name in sa.STATUS.items():
+        assert L.attn_status_name(code).decode() == name
+    assert sa.sage_padded_len(1) == 128 and sa.sage_padded_len(128) == 128 and sa.sage_padded_len(129) == 256
+    assert sa.sage_padded_len(76112) == 76160 and sa.sage_padded_len(119056) == 119168
+    assert L.sage_prepare_workspace_size(2, 3) == 2 * 3 * 128 * 4
+    assert L.sage_attn_workspace_size(1, 40, 76160) == 4 * 40 * 76160 * 128
+
+
+FAKE = 0x10000  # an aligned non-null address; validation never dereferences it
+
+
+def call_fwd(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, S=256, H=2, D=128, qs=(256 * 2 * 128, 256, 128), scale=0.088):
+    L = sa.lib()
+    st = I64x3(*qs)
+    return L.attn_fwd_bf16(q, k, v, o, B, S, H, D, st, st, st, st, scale, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), 3),
+    (dict(B=0), 1),
+    (dict(S=0), 1),
+    (dict(H=-1), 1),
+    (dict(q=0), 1),
+    (dict(o=FAKE + 8), 2),
+    (dict(qs=(256 * 2 * 128, 260, 128)), 2),
+    (dict(qs=(256 * 2 * 128, -256, 128)), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(B=300, H=300), 1),
+])
+def test_attn_fwd_bf16_rejects_bad_arguments(kw, status):
+    assert call_fwd(**kw) == status
+    assert sa.lib().attn_last_error().decode() != ""
+
+
+def call_prepare(rope_dim=0, S_pad=256, qn=None, kn=None, ws_bytes=10**6, cos=None):
+    L = sa.lib()
+    st = I64x3(256 * 2 * 128, 256, 128)
+    return L.sage_prepare(FAKE, FAKE, FAKE, 1, 256, 2, 128, st, st, st, 0.088, qn, kn, 1e-6, cos, cos, rope_dim,
+                          S_pad, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(rope_dim=48, cos=FAKE), 1),
+    (dict(rope_dim=64, cos=None), 1),
+    (dict(S_pad=200), 1),
+    (dict(S_pad=128), 1),
+    (dict(qn=FAKE, kn=None), 1),
+    (dict(qn=FAKE + 4, kn=FAKE), 2),
+    (dict(ws_bytes=16), 1),
+])
+def test_sage_prepare_rejects_bad_arguments(kw, status):
+    assert call_prepare(**kw) == status
+
+
+def test_sage_attn_fwd_rejects_bad_arguments():
+    L = sa.lib()
+    st = I64x3(256 * 2 * 128, 256, 128)
+    ok_ws = L.sage_attn_workspace_size(1, 2, 256)
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 128, 192, FAKE, ok_ws, None) == 1
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 128, 256, FAKE, 64, None) == 1
+    assert L.sage_attn_fwd(FAKE, FAKE + 1, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 128, 256, FAKE, ok_ws,
+                           None) == 2
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 96, 256, FAKE, ok_ws, None) == 3
+
+
+def test_product_path_does_not_import_the_oracle():
+    import subprocess
+    import sys
+    code = ("import sys, sage_attention_forward_gb300 as s; s.lib(); "
+            "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules), 'oracle imported'")
+    subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)

@@ -1,0 +1,112 @@
+"""sage_prepare (CUDA, through the C ABI) is bit-exact against the oracle:
+INT8 Q/K codes, e4m3 V codes and all FP32 scales, on every workload and on
+small ragged shapes, with and without the fused RMSNorm + RoPE."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sage_attention_forward_gb300 as sa
+from workloads import make_inputs, rope_tables, small_case, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def assert_prepared_equal(prep, exp, what=""):
+    for name in ("q_i8", "k_i8", "v_fp8", "q_scale", "k_scale", "v_scale"):
+        got = getattr(prep, name).cpu()
+        ref = exp[name]
+        if got.dtype == torch.float32:
+            same = torch.equal(got.view(torch.int32), ref.view(torch.int32))
+        else:
+            same = torch.equal(got, ref)
+        if not same:
+            diff = (got.view(torch.uint8) != ref.view(torch.uint8)) if got.dtype != torch.float32 else (got != ref)
+            idx = diff.nonzero()[:5].tolist()
+            raise AssertionError(f"{what}: {name} differs at {int(diff.sum())} places, first {idx}")
+
+
+def run(inp, dev, S_pad=None, **kw):
+    g = to_device(inp, dev)
+    norm = {}
+    if g.q_norm_w is not None:
+        norm = dict(q_norm_w=g.q_norm_w, k_norm_w=g.k_norm_w, rms_eps=inp.wl.rms_eps)
+    rope = {}
+    if g.rope_cos is not None:
+        rope = dict(rope_cos=g.rope_cos, rope_sin=g.rope_sin, rope_dim=inp.wl.rope_dim)
+    prep = sa.sage_prepare(g.q, g.k, g.v, softmax_scale=inp.wl.softmax_scale, S_pad=S_pad, **norm, **rope, **kw)
+    torch.cuda.synchronize()
+    exp = oracle.prepare(inp.q, inp.k, inp.v, inp.wl.softmax_scale, S_pad=prep.S_pad,
+                         q_norm_w=inp.q_norm_w, k_norm_w=inp.k_norm_w, rms_eps=inp.wl.rms_eps,
+                         rope_cos=inp.rope_cos, rope_sin=inp.rope_sin, rope_dim=inp.wl.rope_dim)
+    return prep, exp
+
+
+@pytest.mark.parametrize("B,H,S", [(1, 1, 1), (1, 3, 31), (2, 1, 33), (1, 2, 127), (1, 3, 129), (2, 2, 200),
+                                   (1, 1, 1000)])
+def test_small_ragged_bit_exact(cuda_dev, B, H, S):
+    inp = make_inputs(small_case(B, H, S, 200 + S))
+    prep, exp = run(inp, cuda_dev)
+    assert_prepared_equal(prep, exp, f"B{B} H{H} S{S}")
+
+
+def test_extra_padding_is_zero(cuda_dev):
+    inp = make_inputs(small_case(1, 2, 100, 3))
+    prep, exp = run(inp, cuda_dev, S_pad=512)
+    assert_prepared_equal(prep, exp, "S_pad 512")
+    assert (prep.q_i8[:, :, 100:] == 0).all() and (prep.v_fp8[..., 100:] == 0).all()
+
+
+@pytest.mark.parametrize("rope_dim", [0, 32, 64, 96, 128])
+@pytest.mark.parametrize("norm", [False, True])
+def test_norm_rope_bit_exact(cuda_dev, rope_dim, norm):
+    if rope_dim == 0 and not norm:
+        pytest.skip("covered by the plain cases")
+    inp = make_inputs(small_case(2, 3, 300, 300 + rope_dim, rms_norm=norm, rope_dim=rope_dim))
+    prep, exp = run(inp, cuda_dev)
+    assert_prepared_equal(prep, exp, f"norm={norm} rope_dim={rope_dim}")
+
+
+def test_fused_equals_unfused(cuda_dev):
+    """Prepare with RMSNorm + RoPE fused equals prepare without them applied to the
+    normalised, rotated BF16 tensors (aiter pull request, Test Result: fused == unfused)."""
+    inp = make_inputs(small_case(1, 4, 500, 41, rms_norm=True, rope_dim=64))
+    prep, _ = run(inp, cuda_dev)
+    qn = oracle.norm_rope(inp.q, inp.q_norm_w, inp.wl.rms_eps, inp.rope_cos, inp.rope_sin, 64).to(cuda_dev)
+    kn = oracle.norm_rope(inp.k, inp.k_norm_w, inp.wl.rms_eps, inp.rope_cos, inp.rope_sin, 64).to(cuda_dev)
+    plain = sa.sage_prepare(qn, kn, inp.v.to(cuda_dev), softmax_scale=inp.wl.softmax_scale)
+    torch.cuda.synchronize()
+    for name in ("q_i8", "k_i8", "v_fp8", "q_scale", "k_scale", "v_scale"):
+        assert torch.equal(getattr(prep, name), getattr(plain, name)), name
+
+
+@pytest.mark.parametrize("name", ["tiny", "flux1024", "flux2048", "wan720p", "hunyuan720p"])
+def test_workloads_bit_exact(cuda_dev, workload_inputs, name):
+    cpu, g = workload_inputs(name)
+    kw = {}
+    if g.q_norm_w is not None:
+        kw.update(q_norm_w=g.q_norm_w, k_norm_w=g.k_norm_w, rms_eps=cpu.wl.rms_eps)
+    if g.rope_cos is not None:
+        kw.update(rope_cos=g.rope_cos, rope_sin=g.rope_sin, rope_dim=cpu.wl.rope_dim)
+    prep = sa.sage_prepare(g.q, g.k, g.v, softmax_scale=cpu.wl.softmax_scale, **kw)
+    torch.cuda.synchronize()
+    exp = oracle.prepare(cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, S_pad=prep.S_pad, q_norm_w=cpu.q_norm_w,
+                         k_norm_w=cpu.k_norm_w, rms_eps=cpu.wl.rms_eps, rope_cos=cpu.rope_cos,
+                         rope_sin=cpu.rope_sin, rope_dim=cpu.wl.rope_dim)
+    assert_prepared_equal(prep, exp, name)
+
+
+def test_deterministic_non_default_stream(cuda_dev):
+    inp = make_inputs(small_case(1, 3, 777, 42, rms_norm=True, rope_dim=32))
+    g = to_device(inp, cuda_dev)
+    kw = dict(q_norm_w=g.q_norm_w, k_norm_w=g.k_norm_w, rope_cos=g.rope_cos, rope_sin=g.rope_sin, rope_dim=32)
+    a = sa.sage_prepare(g.q, g.k, g.v, **kw)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = sa.sage_prepare(g.q, g.k, g.v, stream=s, **kw)
+    s.synchronize()
+    torch.cuda.synchronize()
+    for name in ("q_i8", "k_i8", "v_fp8", "q_scale", "k_scale", "v_scale"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
