@@ -1,0 +1,370 @@
+"""Throughput benchmark of the attention forward on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch of synthetic input at the
+Wan-2.1-720p shape (B=1, H=40, S=76112, D=128, 5 % outlier tokens x8):
+    attn_fwd_bf16(Q, K, V)            BF16 flash attention
+    sage_prepare(Q, K, V)             INT8 Q/K, e4m3 V
+    sage_attn_fwd(prepared)           INT8 QK^T / FP8 PV attention
+The metric is attention TFLOPS, 4*B*H*S^2*D per attention evaluation; a step
+evaluates attention twice (BF16 and Sage), so value = 2 * 4*B*H*S^2*D * steps
+/ time, summed over ranks.  Per-call times and TFLOPS are reported under
+"providers".  Inputs are resident in HBM and larger than L2 (779 MB each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (FP64 attention, plain C) on the host
+cores, on bounded row samples of the same workload, in the same metric.
+Under torchrun (N > 1) every rank runs an independent replica (the op has no
+exchange step); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPS (4·B·H·S²·D/s) at S=76112,H=40,D=128; % of tensor peak"
+KERNELS_PER_STEP = 5  # attn_bf16, prep_qk_vmax, prep_v, widen_i8_f16, sage_attn
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(bf16=float(p["bf16_tflops"]), bf16_sustained=float(p["bf16_tflops_sustained"]),
+                    hbm=float(p["hbm_gbs"]), source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args, rank, world):
+    import torch
+    import sage_attention_forward_gb300 as sa
+    from sage_attention_forward_gb300 import roofline
+    from workloads import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    B, H, S, D = wl.B, wl.H, wl.S, wl.D
+    inp = make_inputs(wl, device=dev)          # drawn on the device: inputs resident in HBM
+    q, k, v = inp.q, inp.k, inp.v
+    scale = wl.softmax_scale
+    S_pad = sa.sage_padded_len(S)
+    o_bf16 = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+    o_sage = torch.empty_like(o_bf16)
+    prep = sa.Prepared.empty(B, H, S, S_pad, dev)
+    ws_p = sa.prepare_workspace(B, H, dev)
+    ws_a = sa.attn_workspace(B, H, S_pad, dev)
+    kw = {}
+    if inp.q_norm_w is not None:
+        kw.update(q_norm_w=inp.q_norm_w, k_norm_w=inp.k_norm_w, rms_eps=wl.rms_eps)
+    if inp.rope_cos is not None:
+        kw.update(rope_cos=inp.rope_cos, rope_sin=inp.rope_sin, rope_dim=wl.rope_dim)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale)
+        if ev is not None:
+            ev[1].record(stream)
+        sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw)
+        if ev is not None:
+            ev[2].record(stream)
+        sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)
+        if ev is not None:
+            ev[3].record(stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    sa.attn_get_device_status()
+    barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        barrier()
+    sa.attn_get_device_status()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    per = {"bf16": [], "prepare": [], "sage_core": []}
+    for e in evs:
+        per["bf16"].append(e[0].elapsed_time(e[1]))
+        per["prepare"].append(e[1].elapsed_time(e[2]))
+        per["sage_core"].append(e[2].elapsed_time(e[3]))
+    F = roofline.attention_flops(B, H, S, D)
+    ms = {k2: statistics.mean(v2) for k2, v2 in per.items()}
+    ms["sage"] = ms["prepare"] + ms["sage_core"]
+    prep_bytes = roofline.prepare_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
+    peaks = load_peaks()
+    bf16_tflops = F / (ms["bf16"] * 1e-3) / 1e12
+    providers = {
+        "bf16": {"ms": ms["bf16"], "tflops": bf16_tflops},
+        "sage": {"ms": ms["sage"], "tflops": F / (ms["sage"] * 1e-3) / 1e12},
+        "sage_core": {"ms": ms["sage_core"], "tflops": F / (ms["sage_core"] * 1e-3) / 1e12,
+                      # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
+                      "frac_of_tensor_roof": (F / (ms["sage_core"] * 1e-3) / 1e12) /
+                      (peaks["bf16_sustained"] / 0.75)},
+        "prepare": {"ms": ms["prepare"], "gbs": prep_bytes / (ms["prepare"] * 1e-3) / 1e9,
+                    "frac_of_hbm": prep_bytes / (ms["prepare"] * 1e-3) / 1e9 / peaks["hbm"]},
+    }
+
+    # ------------------------------------------------------------- end to end
+    e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)
+
+    result = {
+        "metric": METRIC,
+        "value": world * 2 * F * args.steps / (elapsed_ms * 1e-3) / 1e12,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16+int8/e4m3",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name}: B={B} H={H} S={S} D={D}"
+                               + (", 5% outlier tokens x8" if wl.outlier_frac else ""),
+                   "B": B, "H": H, "S": S, "D": D,
+                   "step": "attn_fwd_bf16 + sage_prepare + sage_attn_fwd (two attention evaluations)",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "providers": providers,
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": bf16_tflops,
+                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": bf16_tflops / peaks["bf16_sustained"], "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 sustained"},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": e2e,
+    }
+    result["clocks"] = clk.summary()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    return result
+
+
+def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
+    """Same step through the public API from pinned host buffers: H2D of Q, K, V,
+    both attention paths, D2H of both outputs, every step inside the timed region."""
+    B, S, H, D = inp.q.shape
+    hq = inp.q.contiguous().cpu().pin_memory()
+    hk = inp.k.contiguous().cpu().pin_memory()
+    hv = inp.v.contiguous().cpu().pin_memory()
+    ho1 = torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory()
+    ho2 = torch.empty_like(ho1).pin_memory()
+    dq, dk, dv = (torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    o1 = torch.empty_like(dq)
+    o2 = torch.empty_like(dq)
+    prep = sa.Prepared.empty(B, H, S, S_pad, dev)
+    ws_p = sa.prepare_workspace(B, H, dev)
+    ws_a = sa.attn_workspace(B, H, S_pad, dev)
+    kw2 = dict(kw)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        sa.attn_fwd_bf16(dq, dk, dv, out=o1, softmax_scale=scale)
+        sa.sage_prepare(dq, dk, dv, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw2)
+        sa.sage_attn_fwd(prep, out=o2, workspace=ws_a)
+        ho1.copy_(o1, non_blocking=True)
+        ho2.copy_(o2, non_blocking=True)
+
+    steps = max(1, min(args.steps, 3))
+    step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    in_bytes = 3 * hq.numel() * 2
+    out_bytes = 2 * ho1.numel() * 2
+    return {"value": world * 2 * F * steps / (ms * 1e-3) / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_rows(wl, n, seed):
+    import torch
+    from workloads import sample_rows
+    return sample_rows(wl, n, seed=seed, must_include_tail=False)
+
+
+def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
+    """Time the oracle's FP64 attention on sampled query rows of the workload
+    (every row a full softmax over all S keys), on all host cores."""
+    import oracle
+    from workloads import make_inputs
+    from sage_attention_forward_gb300 import roofline
+
+    if inputs is None:
+        inputs = make_inputs(wl)
+    q, k, v = inputs.q, inputs.k, inputs.v
+    per_row = roofline.attention_flops(1, 1, wl.S, wl.D) / wl.S      # 4*S*D per query row
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, wl.softmax_scale, rows=_oracle_rows(wl, 64, 1))
+    dt = time.perf_counter() - t0
+    n = max(64, int(64 * seconds / max(dt, 1e-3)))
+    rows = _oracle_rows(wl, n, 2)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, wl.softmax_scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": n * per_row / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on bounded samples of the same workload."""
+    import oracle
+    from workloads import WORKLOADS, make_inputs
+    from sage_attention_forward_gb300 import roofline
+
+    wl = WORKLOADS[args.workload]
+    inputs = make_inputs(wl)
+    per_row = roofline.attention_flops(1, 1, wl.S, wl.D) / wl.S
+    rows_per_step = args.ref_rows
+    for i in range(args.warmup):
+        oracle.attention(inputs.q, inputs.k, inputs.v, wl.softmax_scale, rows=_oracle_rows(wl, 32, 100 + i))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.attention(inputs.q, inputs.k, inputs.v, wl.softmax_scale, rows=_oracle_rows(wl, rows_per_step, 200 + i))
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps * per_row / dt / 1e12
+    sample = (f"{rows_per_step} query rows per step of {wl.name} (each a full FP64 softmax over S={wl.S} keys); "
+              f"{args.steps} steps in {dt:.1f} s")
+    return {"metric": METRIC, "value": value, "unit": "TFLOPS", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} S={wl.S} D={wl.D}", "B": wl.B, "H": wl.H,
+                       "S": wl.S, "D": wl.D, "step": "CPU oracle, FP64 attention on sampled query rows"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="wan720p")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -21,6 +21,10 @@ Functions and the passages they follow:
   quant_v        -- V to FP8 e4m3 transposed to [B, H, 128, S_pad], one FP32
                     scale per channel (same pull request, Technical Details).
   prepare        -- the three above in order, as the prepare stage runs them.
+  sage_attention -- FP64 attention evaluated on prepared tensors: the exact
+                    value of the INT8/e4m3 format the Sage forward consumes
+                    (same pull request, commit message of
+                    gfx1201_sage_attention), with no further rounding.
   e4m3_encode / e4m3_decode / f32_to_bf16 -- the scalar encoders.
 """
 from __future__ import annotations
@@ -55,6 +59,9 @@ def lib():
         L.oracle_e4m3_encode_array.argtypes = [c_p, c_p, ctypes.c_int64]
         L.oracle_e4m3_decode_array.argtypes = [c_p, c_p, ctypes.c_int64]
         L.oracle_f32_to_bf16_array.argtypes = [c_p, c_p, ctypes.c_int64]
+        L.oracle_sage_attention.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, c_p,
+                                            ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_init()
         _lib = L
@@ -163,6 +170,33 @@ def prepare(q, k, v, softmax_scale, S_pad=None, q_norm_w=None, k_norm_w=None, rm
     v_fp8, v_scale = quant_v(v, S_pad)
     return dict(q_i8=q_i8, k_i8=k_i8, v_fp8=v_fp8, q_scale=q_scale, k_scale=k_scale, v_scale=v_scale,
                 q_pre=q_pre.contiguous(), k_pre=k_pre.contiguous(), S_pad=S_pad, log2_factor=c)
+
+
+def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool = False, p_e4m3: bool = False,
+                   nthreads: int = 0) -> np.ndarray:
+    """FP64 attention of the prepared codes (dict as returned by prepare(), CPU
+    tensors) for query rows (b, s, h) -> [n, 128] float64.  p_e4m3 also rounds
+    the probabilities to e4m3 (448 * w) in the numerator, as the FP8 P V product
+    of the Sage forward needs; abs_v weights |V| instead of V."""
+    q8 = np.ascontiguousarray(prep["q_i8"].numpy())
+    k8 = np.ascontiguousarray(prep["k_i8"].numpy())
+    v8 = np.ascontiguousarray(prep["v_fp8"].numpy())
+    qs = np.ascontiguousarray(prep["q_scale"].numpy())
+    ks = np.ascontiguousarray(prep["k_scale"].numpy())
+    vs = np.ascontiguousarray(prep["v_scale"].numpy())
+    B, _, S_pad, _ = q8.shape
+    r = rows.to(torch.int64)
+    flat = ((r[:, 0] * S + r[:, 1]) * H + r[:, 2]).contiguous().numpy()
+    out = np.empty((len(flat), 128), dtype=np.float64)
+    lib().oracle_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs), _ptr(ks), _ptr(vs), B, S, H, int(S_pad),
+                                _ptr(flat), len(flat), int(abs_v), int(p_e4m3), _ptr(out), int(nthreads))
+    return out
+
+
+def all_rows(B: int, S: int, H: int) -> torch.Tensor:
+    """Every (b, s, h) query row, in [B, S, H] order."""
+    b, s, h = torch.meshgrid(torch.arange(B), torch.arange(S), torch.arange(H), indexing="ij")
+    return torch.stack([b.flatten(), s.flatten(), h.flatten()], dim=1)
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:

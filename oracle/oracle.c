@@ -351,6 +351,72 @@ void oracle_quant_v(const uint16_t* x, int B, int S, int H, int64_t S_pad, uint8
     }
 }
 
+/* ---------------------------------- the exact result of the Sage format */
+
+/*
+ * FP64 attention on prepared tensors, the function the Sage forward
+ * approximates (aiter pull request "gfx1201_sage_prepare /
+ * gfx1201_sage_attention", commit message of gfx1201_sage_attention: scores
+ * from the INT8 codes, Q's scale carrying softmax_scale * log2(e), V from its
+ * e4m3 codes and per-channel scales):
+ *   t_j = (sum_d q_i8[r, d] k_i8[j, d]) * q_scale[r / 32] * k_scale[j / 32]   (log2 units)
+ *   O[r, d] = sum_{j < S} 2^(t_j - max t) v[j, d] / sum_{j < S} 2^(t_j - max t),
+ *   v[j, d] = e4m3(v_fp8[d, j]) * v_scale[d]
+ * with nothing rounded.  p_e4m3 != 0 adds the one rounding the forward's FP8
+ * P V product needs (same commit message: "FP8 WMMA for P V"); reading: the
+ * weights w_j = 2^(t_j - max t) in (0, 1] enter the numerator as
+ * e4m3(448 w_j) / 448 while the denominator sums the unrounded w_j.
+ * abs_v != 0 evaluates the same weights on |v| instead (the weighted mean
+ * magnitude the rounding bounds of the tests scale with).
+ * Layouts: codes [B, H, S_pad, 128] and [B, H, 128, S_pad], scales
+ * [B, H, S_pad/32] and [B, H, 128].  rows: flattened (b*S + s)*H + h.
+ */
+void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8, const float* qs,
+                           const float* ks, const float* vs, int B, int S, int H, int64_t S_pad, const int64_t* rows,
+                           int64_t n_rows, int abs_v, int p_e4m3, double* out, int nthreads) {
+    int64_t nblk = S_pad / 32;
+    (void)B;
+    (void)nthreads;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    e4m3_init();
+#pragma omp parallel
+    {
+        double* t = (double*)malloc(sizeof(double) * (size_t)S);
+        double acc[128];
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; i++) {
+            int64_t r = rows[i];
+            int64_t h = r % H, s = (r / H) % S, b = r / ((int64_t)H * S);
+            int64_t bh = b * H + h;
+            const int8_t* qrow = q8 + (bh * S_pad + s) * 128;
+            double fq = (double)qs[bh * nblk + s / 32];
+            double tmax = -INFINITY;
+            for (int64_t j = 0; j < S; j++) {
+                const int8_t* krow = k8 + (bh * S_pad + j) * 128;
+                int64_t dot = 0;
+                for (int d = 0; d < 128; d++) dot += (int64_t)qrow[d] * (int64_t)krow[d];
+                t[j] = (double)dot * fq * (double)ks[bh * nblk + j / 32];
+                if (t[j] > tmax) tmax = t[j];
+            }
+            double wsum = 0.0;
+            for (int d = 0; d < 128; d++) acc[d] = 0.0;
+            for (int64_t j = 0; j < S; j++) {
+                double w = exp2(t[j] - tmax);
+                wsum += w;
+                if (p_e4m3) w = oracle_e4m3_decode(oracle_e4m3_encode((float)(448.0 * w))) / 448.0;
+                for (int d = 0; d < 128; d++) {
+                    double vv = oracle_e4m3_decode(v8[(bh * 128 + d) * S_pad + j]) * (double)vs[bh * 128 + d];
+                    acc[d] += w * (abs_v ? fabs(vv) : vv);
+                }
+            }
+            for (int d = 0; d < 128; d++) out[i * 128 + d] = acc[d] / wsum;
+        }
+        free(t);
+    }
+}
+
 void oracle_init(void) { e4m3_init(); }
 
 int oracle_num_threads(void) {

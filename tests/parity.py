@@ -1,15 +1,24 @@
-"""Comparison metrics for the GPU parity tests (test helper, not a test file).
+"""Comparison metrics and gates for the GPU parity tests (test helper, not a test file).
 
-Tolerances (written in the tests that use them):
-  BF16 path:  cosine >= 0.99999 and max |O - O_ref| <= 2e-2, where for
-              |O_ref| > 1 the bound scales with |O_ref| (the kernel rounds O
-              and P to BF16, whose step is relative: 2^-8 |x|; on rows of x8
-              outlier tokens |O| reaches ~30 and no BF16 result is within an
-              absolute 2e-2).  The raw max-abs is reported beside it.
-  Sage path:  cosine >= 0.995 and max-abs <= 0.1 with the same scaling.
-Secondary band (aiter pull request "gfx1201_sage_prepare /
-gfx1201_sage_attention", Test Plan): atol 0.3, rtol 0.25 with at most 0.5 %
-of elements outside, cosine >= 0.998 and median row cosine >= 0.99.
+Tolerances, from the arithmetic of each path:
+  BF16 path vs FP64 attention: cosine >= 0.99999 and, elementwise,
+      |O - O_ref| <= 2e-2 + 2^-7 * A|V|
+  where A|V| = sum_j p_j |v_j| / sum_j p_j is the attention-weighted mean
+  magnitude of V (the oracle evaluates it with |V| in place of V).  The
+  kernel rounds every probability to BF16 before the P V product (relative
+  error <= 2^-8 each, so at most 2^-8 A|V| on the output) and rounds O to BF16
+  once more (<= 2^-8 |O| <= 2^-8 A|V|); 2e-2 is the absolute tolerance the
+  acceptance criteria state for everything else.  On rows dominated by a few
+  x8 outlier tokens A|V| reaches ~30, where no BF16 kernel that rounds P can
+  stay within an absolute 2e-2.
+  Sage path vs the exact value of its own format (FP64 attention on the
+  prepared INT8 / e4m3 codes): cosine >= 0.999 and
+      |O - O_fmt| <= 1e-3 + (2^-4 + 2^-8) * A|V|_fmt
+  (e4m3 probabilities, relative error <= 2^-4 each, and the BF16 output).
+  Sage path vs FP64 attention of the BF16 inputs (the acceptance criteria):
+  cosine >= 0.995 and max |O - O_ref| <= 0.1, plus the band of the Sage op's
+  own test plan (aiter pull request, Test Plan: atol 0.3, rtol 0.25, at most
+  0.5 % of elements outside, cosine >= 0.998, median row cosine >= 0.99).
 """
 from __future__ import annotations
 
@@ -17,33 +26,44 @@ import numpy as np
 import torch
 
 
-def metrics(out: torch.Tensor | np.ndarray, ref: np.ndarray) -> dict:
+def metrics(out, ref, bound_scale=None, a=0.0, b=0.0) -> dict:
     o = out.double().cpu().numpy() if isinstance(out, torch.Tensor) else np.asarray(out, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     o2 = o.reshape(-1, o.shape[-1])
     r2 = r.reshape(-1, r.shape[-1])
     d = np.abs(o2 - r2)
-    scaled = d / np.maximum(1.0, np.abs(r2))
     cos = float((o2 * r2).sum() / (np.linalg.norm(o2) * np.linalg.norm(r2) + 1e-300))
     rc = (o2 * r2).sum(1) / (np.linalg.norm(o2, axis=1) * np.linalg.norm(r2, axis=1) + 1e-300)
-    band_fail = float(np.mean(d > 0.3 + 0.25 * np.abs(r2)))
-    return dict(max_abs=float(d.max()), max_scaled=float(scaled.max()), cos=cos, median_row_cos=float(np.median(rc)),
-                min_row_cos=float(rc.min()), rel_l2=float(np.linalg.norm(o2 - r2) / (np.linalg.norm(r2) + 1e-300)),
-                band_fail=band_fail, nan=bool(np.isnan(o2).any()))
+    m = dict(max_abs=float(d.max()), cos=cos, median_row_cos=float(np.median(rc)), min_row_cos=float(rc.min()),
+             rel_l2=float(np.linalg.norm(o2 - r2) / (np.linalg.norm(r2) + 1e-300)),
+             band_fail=float(np.mean(d > 0.3 + 0.25 * np.abs(r2))), nan=bool(np.isnan(o2).any()))
+    if bound_scale is not None:
+        s = np.asarray(bound_scale, dtype=np.float64).reshape(d.shape)
+        m["bound_ratio"] = float((d / (a + b * s)).max())   # <= 1 passes
+    return m
 
 
 def assert_bf16_gate(m: dict, what: str = ""):
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["cos"] >= 0.99999, f"{what}: cosine {m}"
-    assert m["max_scaled"] <= 2e-2, f"{what}: max error {m}"
+    assert m["bound_ratio"] <= 1.0, f"{what}: error above 2e-2 + 2^-7 A|V| {m}"
 
 
-def assert_sage_gate(m: dict, what: str = ""):
+def assert_sage_format_gate(m: dict, what: str = ""):
+    assert not m["nan"], f"{what}: NaN in output {m}"
+    assert m["cos"] >= 0.999, f"{what}: cosine vs format-exact {m}"
+    assert m["bound_ratio"] <= 1.0, f"{what}: error above 1e-3 + (2^-4 + 2^-8) A|V| {m}"
+
+
+def assert_sage_exact_gate(m: dict, what: str = ""):
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["cos"] >= 0.995, f"{what}: cosine {m}"
-    assert m["max_scaled"] <= 0.1, f"{what}: max error {m}"
-    # secondary band of the Sage op's own test plan
+    assert m["max_abs"] <= 0.1, f"{what}: max-abs {m}"
     assert m["band_fail"] <= 0.005 and m["cos"] >= 0.998 and m["median_row_cos"] >= 0.99, f"{what}: band {m}"
+
+
+BF16_A, BF16_B = 2e-2, 2.0 ** -7
+SAGE_A, SAGE_B = 1e-3, 2.0 ** -4 + 2.0 ** -8
 
 
 def gather_rows(o: torch.Tensor, rows: torch.Tensor) -> np.ndarray:

