@@ -50,7 +50,7 @@ struct __align__(1024) Smem {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[kNQ];
-  uint64_t p_full[kNQ];
+  uint64_t p_full[kNQ][2];   // P_i keys [0,64) and [64,128) stored in TMEM
   uint64_t o_done[kNQ];
   uint64_t mma_drain;
   uint32_t tmem_base;
@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNQ; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_full[i][0], 4);
+      mbar_init(&sm.p_full[i][1], 4);
       mbar_init(&sm.o_done[i], 1);
     }
     mbar_init(&sm.mma_drain, 1);
@@ -158,15 +159,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int i, int slot, bool acc) {
+      // O_i += P_i V for keys [64*half, 64*half + 64): 4 steps of 16 keys, i.e. rows
+      // kk*16.. of the [key][d] tile; the two 64-column halves of d sit kHalfBytes
+      // apart (LBO), 8-row groups 1024 bytes apart (SBO)
+      auto issue_pv_half = [&](int i, int slot, int half, bool acc) {
         const uint32_t va = smem_u32(sm.kv[slot]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // 16 keys per step: rows kk*16.. of the [key][d] tile; the two 64-column
-          // halves of d sit kHalfBytes apart (LBO), 8-row groups 1024 bytes apart (SBO)
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * half + k4;
           mma_f16_ts(tO(i), tS(i) + kk * 8, smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024), idesc_pv,
                      (acc || kk > 0) ? 1u : 0u);
         }
+      };
+      // wait for each half of P_i, issue its four MMAs, then signal O_i done
+      auto issue_pv = [&](int i, int slot, int j) -> bool {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (!mbar_wait(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
+          tc_fence_after();
+          issue_pv_half(i, slot, half, j > 0);
+        }
+        mma_commit(&sm.o_done[i]);
+        return true;
       };
 
       bool ok = mbar_wait(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
@@ -184,20 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int itK = 2 * j + 2, slotK = itK % kStages;
         const bool more = (j + 1 < n);
         if (!mbar_wait(&sm.kv_full[slotV], (itV / kStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
-        if (!mbar_wait(&sm.p_full[0], j & 1, abort_flag, err, kErrTimeoutSync)) break;
-        tc_fence_after();
-        issue_pv(0, slotV, j > 0);
-        mma_commit(&sm.o_done[0]);
+        if (!issue_pv(0, slotV, j)) break;
         if (more) {
           if (!mbar_wait(&sm.kv_full[slotK], (itK / kStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
           tc_fence_after();
           issue_s(0, slotK);
           mma_commit(&sm.s_full[0]);
         }
-        if (!mbar_wait(&sm.p_full[1], j & 1, abort_flag, err, kErrTimeoutSync)) break;
-        tc_fence_after();
-        issue_pv(1, slotV, j > 0);
-        mma_commit(&sm.o_done[1]);
+        if (!issue_pv(1, slotV, j)) break;
         mma_commit(&sm.kv_empty[slotV]);
         if (more) {
           issue_s(1, slotK);
@@ -237,10 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 128; ++e)
           if (e >= valid) s[e] = f2u(-INFINITY);
       }
-      float mx = fmax3(u2f(s[0]), u2f(s[1]), u2f(s[2]));
-#pragma unroll
-      for (int e = 3; e < 127; e += 2) mx = fmax3(mx, u2f(s[e]), u2f(s[e + 1]));
-      mx = fmaxf(mx, u2f(s[127]));
+      const float mx = fmaxf(fmaxf(max32(&s[0]), max32(&s[32])), fmaxf(max32(&s[64]), max32(&s[96])));
       const float m_cand = mx * c;
       const bool need = m_cand > m_used + kTau;
       // a row whose tile maximum passed its reference by more than kTau moves the
@@ -265,30 +270,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + 16 * cc, pk);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_i must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already stored)
-        if (!mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+        if (cc & 1) {
+          if (cc == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
+            // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
+            // before the first half of P_j V_j accumulates into it
+            if (mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+              tc_fence_after();
+#pragma unroll
+              for (int c2 = 0; c2 < 8; ++c2) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16 * c2, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
+                tmem_st16(tO + 16 * c2, o);
+              }
+            } else {
+              ok = false;
+            }
+          }
+          // keys [0,64) then [64,128) of P_i are ready: the PV MMA on them may start
           tmem_st_wait();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * cc, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * sc);
-          tmem_st32(tO + 32 * cc, o);
+          tc_fence_before();
+          __syncwarp();
+          if (ok && lane == 0) mbar_arrive(&sm.p_full[i][cc >> 1]);
         }
       }
-      tmem_st_wait();
+      if (!ok) break;
       l += rs0 + rs1;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[i]);
     }
 
     if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {

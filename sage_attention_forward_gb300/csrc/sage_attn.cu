@@ -58,7 +58,7 @@ struct __align__(1024) Smem {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[kNQ];
-  uint64_t p_full[kNQ];
+  uint64_t p_full[kNQ][2];   // P_i keys [0,64) and [64,128) stored in TMEM
   uint64_t o_done[kNQ];
   uint64_t mma_drain;
   uint32_t tmem_base;
@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNQ; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_full[i][0], 4);
+      mbar_init(&sm.p_full[i][1], 4);
       mbar_init(&sm.o_done[i], 1);
     }
     mbar_init(&sm.mma_drain, 1);
@@ -184,14 +185,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int i, int slot, bool acc) {
+      // O_i += P_i V for keys [64*half, 64*half + 64): 2 steps of 32 positions (bytes)
+      // inside the 128-byte swizzled rows of V^T
+      auto issue_pv_half = [&](int i, int slot, int half, bool acc) {
         const uint32_t va = smem_u32(sm.v[slot]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // 32 positions (bytes) per step inside the 128-byte swizzled rows of V^T
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int kk = 2 * half + k2;
           mma_f8_ts(tO(i), tS(i) + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), idesc_pv,
                     (acc || kk > 0) ? 1u : 0u);
         }
+      };
+      auto issue_pv = [&](int i, int slot, int j) -> bool {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (!mbar_wait(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
+          tc_fence_after();
+          issue_pv_half(i, slot, half, j > 0);
+        }
+        mma_commit(&sm.o_done[i]);
+        return true;
       };
 
       bool ok = mbar_wait(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
@@ -209,20 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slotK = (j + 1) % kKStages;
         const bool more = (j + 1 < n);
         if (!mbar_wait(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
-        if (!mbar_wait(&sm.p_full[0], j & 1, abort_flag, err, kErrTimeoutSync)) break;
-        tc_fence_after();
-        issue_pv(0, slotV, j > 0);
-        mma_commit(&sm.o_done[0]);
+        if (!issue_pv(0, slotV, j)) break;
         if (more) {
           if (!mbar_wait(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
           tc_fence_after();
           issue_s(0, slotK);
           mma_commit(&sm.s_full[0]);
         }
-        if (!mbar_wait(&sm.p_full[1], j & 1, abort_flag, err, kErrTimeoutSync)) break;
-        tc_fence_after();
-        issue_pv(1, slotV, j > 0);
-        mma_commit(&sm.o_done[1]);
+        if (!issue_pv(1, slotV, j)) break;
         mma_commit(&sm.v_empty[slotV]);
         if (more) {
           issue_s(1, slotK);
@@ -264,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_ld_wait();
       // keys past S: excluded from the maximum here and given probability 0 below
-      // (their scale may be 0, and 0 * -inf would be NaN)
       const int valid = p.S - j * kBN;
       if (valid < kBN) {
 #pragma unroll
@@ -274,13 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_cand = -INFINITY;
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
-        float mx = fmax3(u2f(s[32 * blk]), u2f(s[32 * blk + 1]), u2f(s[32 * blk + 2]));
-#pragma unroll
-        for (int e = 3; e < 31; e += 2) mx = fmax3(mx, u2f(s[32 * blk + e]), u2f(s[32 * blk + e + 1]));
-        mx = fmaxf(mx, u2f(s[32 * blk + 31]));
         // scales are >= 0, so the block's largest t is f * (largest raw score); a block
         // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
-        m_cand = fmaxf(m_cand, mx * f[blk]);
+        m_cand = fmaxf(m_cand, max32(&s[32 * blk]) * f[blk]);
       }
       const bool need = m_cand > m_used + kTau;
       // a row whose tile maximum passed its reference by more than kTau moves the
@@ -303,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p2 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 2]), f[blk], -off));
           float p3 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 3]), f[blk], -off));
           if (valid < kBN) {
+            // keys past S: probability 0 (their scale may be 0, and 0 * -inf is NaN)
             const int c0 = 32 * blk + 4 * e;
             p0 = c0 + 0 < valid ? p0 : 0.0f;
             p1 = c0 + 1 < valid ? p1 : 0.0f;
@@ -314,30 +317,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e] = pack_e4m3x4(p0, p1, p2, p3);
         }
         tmem_st8(tS + 8 * blk, pk);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_i must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already stored)
-        if (!mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+        if (blk & 1) {
+          if (blk == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
+            // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
+            // before the first half of P_j V_j accumulates into it
+            if (mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+              tc_fence_after();
+#pragma unroll
+              for (int c2 = 0; c2 < 8; ++c2) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16 * c2, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
+                tmem_st16(tO + 16 * c2, o);
+              }
+            } else {
+              ok = false;
+            }
+          }
+          // keys [0,64) then [64,128) of P_i are ready: the PV MMA on them may start
           tmem_st_wait();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * cc, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * sc);
-          tmem_st32(tO + 32 * cc, o);
+          tc_fence_before();
+          __syncwarp();
+          if (ok && lane == 0) mbar_arrive(&sm.p_full[i][blk >> 1]);
         }
       }
-      tmem_st_wait();
+      if (!ok) break;
       l += rs0 + rs1;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[i]);
     }
 
     if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
