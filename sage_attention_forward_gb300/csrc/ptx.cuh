@@ -221,6 +221,20 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t a_fmt, uint32_t b_f
 constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtE4M3 = 0;
 
 // ----------------------------------------------------------------- MMA issue
+// One lane of a fully active warp (elect.sync picks the lowest active lane, so
+// it is the same lane every time).  The tcgen05 issue loops run on the whole
+// warp -- descriptors and loop state are then warp-uniform -- and only the
+// issuing instructions are predicated on this.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T  (both operands described by descriptors)
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {

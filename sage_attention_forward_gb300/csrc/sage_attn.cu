@@ -167,7 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    if (lane == 0) {
+    {
+      // the whole warp runs the issue loop (descriptors and loop state stay
+      // warp-uniform, which keeps each tcgen05.mma issue cheap); one elected
+      // lane issues every tcgen05 instruction
+      const bool leader = elect_one();
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_qk = idesc_f32acc(kFmtF16, kFmtF16, false, false, kBM, kBN);
       const uint32_t idesc_pv = idesc_f32acc(kFmtE4M3, kFmtE4M3, false, false, kBM, 128);
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_f16_ss(tS(i), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_qk,
-                     kk > 0 ? 1u : 0u);
+          const uint64_t da = smem_desc_sw128(qa + off, 16, 1024), db = smem_desc_sw128(ka + off, 16, 1024);
+          if (leader) mma_f16_ss(tS(i), da, db, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       // O_i += P_i V for keys [64*half, 64*half + 64): 2 steps of 32 positions (bytes)
@@ -192,52 +196,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
           const int kk = 2 * half + k2;
-          mma_f8_ts(tO(i), tS(i) + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), idesc_pv,
-                    (acc || kk > 0) ? 1u : 0u);
+          const uint64_t db = smem_desc_sw128(va + kk * 32, 16, 1024);
+          if (leader) mma_f8_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int i, int slot, int j) -> bool {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
+          if (!mbar_wait_warp(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
           tc_fence_after();
           issue_pv_half(i, slot, half, j > 0);
         }
-        mma_commit(&sm.o_done[i]);
+        if (leader) mma_commit(&sm.o_done[i]);
         return true;
       };
 
-      bool ok = mbar_wait(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
-      if (ok) ok = mbar_wait(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
+      bool ok = mbar_wait_warp(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait_warp(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
-        mma_commit(&sm.s_full[0]);
+        if (leader) mma_commit(&sm.s_full[0]);
         issue_s(1, 0);
-        mma_commit(&sm.s_full[1]);
-        mma_commit(&sm.k_empty[0]);
+        if (leader) mma_commit(&sm.s_full[1]);
+        if (leader) mma_commit(&sm.k_empty[0]);
       }
       for (int j = 0; j < n && ok; ++j) {
         const int slotV = j % kVStages;
         const int slotK = (j + 1) % kKStages;
         const bool more = (j + 1 < n);
-        if (!mbar_wait(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+        if (!mbar_wait_warp(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
         if (!issue_pv(0, slotV, j)) break;
         if (more) {
-          if (!mbar_wait(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+          if (!mbar_wait_warp(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
           tc_fence_after();
           issue_s(0, slotK);
-          mma_commit(&sm.s_full[0]);
+          if (leader) mma_commit(&sm.s_full[0]);
         }
         if (!issue_pv(1, slotV, j)) break;
-        mma_commit(&sm.v_empty[slotV]);
+        if (leader) mma_commit(&sm.v_empty[slotV]);
         if (more) {
           issue_s(1, slotK);
-          mma_commit(&sm.s_full[1]);
-          mma_commit(&sm.k_empty[slotK]);
+          if (leader) mma_commit(&sm.s_full[1]);
+          if (leader) mma_commit(&sm.k_empty[slotK]);
         }
       }
-      mma_commit(&sm.mma_drain);
+      if (leader) mma_commit(&sm.mma_drain);
       mbar_wait_teardown(&sm.mma_drain, 0);
     }
   } else {
