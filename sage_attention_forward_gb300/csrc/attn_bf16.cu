@@ -52,6 +52,7 @@ struct __align__(1024) Smem {
   uint64_t s_full[kNQ];
   uint64_t p_full[kNQ][2];   // P_i keys [0,64) and [64,128) stored in TMEM
   uint64_t o_done[kNQ];
+  uint64_t turn[kNQ];        // softmax turn token: the two Q tiles' softmax sections alternate
   uint64_t mma_drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i][0], 4);
       mbar_init(&sm.p_full[i][1], 4);
       mbar_init(&sm.o_done[i], 1);
+      mbar_init(&sm.turn[i], 4);
     }
     mbar_init(&sm.mma_drain, 1);
     sm.abort_flag = 0;
@@ -236,20 +238,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
+      // the two Q tiles' softmax sections alternate (tile 0 of step j, tile 1 of step
+      // j, tile 0 of step j+1, ...), so each runs its exponentials without sharing the
+      // SM sub-partitions' MUFU and issue slots with the other
+      if ((i == 1 || j > 0) &&
+          !mbar_wait_warp(&sm.turn[i], (i == 0 ? j - 1 : j) & 1, abort_flag, err, kErrTimeoutSync)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       uint32_t s[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      tmem_ld_wait();
+      uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+      uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+      uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+      uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
       const int valid = p.S - j * kBN;
-      if (valid < kBN) {
+      float mx;
+      tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld_wait();
+      tmem_reg_fence(s0);
+      tmem_reg_fence(s1);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
+      if (valid >= kBN) {
+        // the first half's maximum overlaps the second half's load
+        const float mx01 = fmaxf(max32(&s[0]), max32(&s[32]));
+        tmem_ld_wait();
+        tmem_reg_fence(s2);
+        tmem_reg_fence(s3);
+        mx = fmaxf(mx01, fmaxf(max32(&s[64]), max32(&s[96])));
+      } else {
+        tmem_ld_wait();
+        tmem_reg_fence(s2);
+        tmem_reg_fence(s3);
 #pragma unroll
         for (int e = 0; e < 128; ++e)
           if (e >= valid) s[e] = f2u(-INFINITY);
+        mx = fmaxf(fmaxf(max32(&s[0]), max32(&s[32])), fmaxf(max32(&s[64]), max32(&s[96])));
       }
-      const float mx = fmaxf(fmaxf(max32(&s[0]), max32(&s[32])), fmaxf(max32(&s[64]), max32(&s[96])));
       const float m_cand = mx * c;
       const bool need = m_cand > m_used + kTau;
       // a row whose tile maximum passed its reference by more than kTau moves the
@@ -267,10 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(u2f(s[32 * cc + 2 * e]), c, neg_m));
-          const float p1 = ex2_approx(fmaf(u2f(s[32 * cc + 2 * e + 1]), c, neg_m));
-          rs0 += p0;
-          rs1 += p1;
+          float x0, x1;
+          ffma2(x0, x1, u2f(s[32 * cc + 2 * e]), u2f(s[32 * cc + 2 * e + 1]), c, c, neg_m, neg_m);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          fadd2(rs0, rs1, rs0, rs1, p0, p1);
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + 16 * cc, pk);
@@ -302,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       l += rs0 + rs1;
+      // hand the turn to the other Q tile's softmax
+      if (lane == 0) mbar_arrive(&sm.turn[i ^ 1]);
     }
 
     if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {

@@ -46,29 +46,46 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Test (kSleep = false) or test-and-sleep (kSleep = true): a sleeping thread may
+// be suspended up to kSuspendNs until the phase completes, so a waiting warp
+// takes no issue slots from working warps on its SM sub-partition, at the
+// price of some wake-up latency.
+constexpr uint32_t kSuspendNs = 1000000;  // 1 ms
+template <bool kSleep>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (kSleep) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
 // Bounded wait for the phase of `bar` with the given parity.  Returns false
 // if the CTA's abort flag is up or the time limit passed; in the latter case
 // it raises the abort flag and records `err` in the kernel's error word.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t* err_word, uint32_t err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kSleep>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (;;) {
+    if (mbar_try_wait<kSleep>(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
       *abort_flag = 1u;
       atomicOr(err_word, err);
       return false;
@@ -78,18 +95,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Warp-uniform form for warps whose next instruction is a warp-collective
 // (.sync.aligned) one: every lane waits, then all lanes take the same branch.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                uint32_t* err_word, uint32_t err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err_word, err);
+  const bool ok = mbar_wait<kSleep>(bar, parity, abort_flag, err_word, err);
   return __all_sync(0xffffffffu, ok);
 }
 
 // Bounded wait used while tearing down after an abort: no abort check.
 __device__ __forceinline__ bool mbar_wait_teardown(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  for (;;) {
+    if (mbar_try_wait<false>(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 
@@ -188,6 +206,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+// After tcgen05.wait::ld: ties the loaded registers to this point so that no
+// use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -280,6 +308,22 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Two binary32 FMAs / adds in one packed instruction (f32x2, sm_100 and later).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

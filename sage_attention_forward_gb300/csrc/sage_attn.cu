@@ -27,6 +27,10 @@
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P_i
 // (e4m3) overwrites the first 32 columns of S_i.  The reference maximum moves
 // only when a tile's maximum exceeds it by more than kTau (log2 units).
+// Unlike the BF16 kernel, the two softmax warpgroups are not made to take
+// turns, and every wait sleeps on its barrier: with the cheaper e4m3 P V
+// product the softmax warps are the busiest units, and overlapping the two
+// warpgroups' sections keeps the SM sub-partitions' issue slots fuller.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n && ok; ++j) {
         {
           const int slot = j % kKStages, use = j / kKStages;
-          if (use > 0 && !mbar_wait(&sm.k_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+          if (use > 0 && !mbar_wait<true>(&sm.k_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
             ok = false;
             break;
           }
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         {
           const int slot = j % kVStages, use = j / kVStages;
-          if (use > 0 && !mbar_wait(&sm.v_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+          if (use > 0 && !mbar_wait<true>(&sm.v_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
             ok = false;
             break;
           }
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int i, int slot, int j) -> bool {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait_warp(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
+          if (!mbar_wait_warp<true>(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
           tc_fence_after();
           issue_pv_half(i, slot, half, j > 0);
         }
@@ -211,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
-      bool ok = mbar_wait_warp(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
-      if (ok) ok = mbar_wait_warp(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
+      bool ok = mbar_wait_warp<true>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait_warp<true>(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -225,10 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slotV = j % kVStages;
         const int slotK = (j + 1) % kKStages;
         const bool more = (j + 1 < n);
-        if (!mbar_wait_warp(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+        if (!mbar_wait_warp<true>(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
         if (!issue_pv(0, slotV, j)) break;
         if (more) {
-          if (!mbar_wait_warp(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+          if (!mbar_wait_warp<true>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
           tc_fence_after();
           issue_s(0, slotK);
           if (leader) mma_commit(&sm.s_full[0]);
@@ -266,27 +270,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 ks4 = ks_next;
       if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
       const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
-      if (!mbar_wait_warp(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
+      if (!mbar_wait_warp<true>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-      tmem_ld_wait();
-      // keys past S: excluded from the maximum here and given probability 0 below
+      uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+      uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+      uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+      uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
       const int valid = p.S - j * kBN;
-      if (valid < kBN) {
+      float m_cand;
+      tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld_wait();
+      tmem_reg_fence(s0);
+      tmem_reg_fence(s1);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
+      // scales are >= 0, so a key block's largest t is f * (largest raw score); a block
+      // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
+      if (valid >= kBN) {
+        // the first half's maximum overlaps the second half's load
+        const float m01 = fmaxf(max32(&s[0]) * f[0], max32(&s[32]) * f[1]);
+        tmem_ld_wait();
+        tmem_reg_fence(s2);
+        tmem_reg_fence(s3);
+        m_cand = fmaxf(m01, fmaxf(max32(&s[64]) * f[2], max32(&s[96]) * f[3]));
+      } else {
+        // keys past S: excluded from the maximum here and given probability 0 below
+        tmem_ld_wait();
+        tmem_reg_fence(s2);
+        tmem_reg_fence(s3);
 #pragma unroll
         for (int e = 0; e < 128; ++e)
           if (e >= valid) s[e] = f2u(-INFINITY);
-      }
-      float m_cand = -INFINITY;
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        // scales are >= 0, so the block's largest t is f * (largest raw score); a block
-        // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
-        m_cand = fmaxf(m_cand, max32(&s[32 * blk]) * f[blk]);
+        m_cand = fmaxf(fmaxf(max32(&s[0]) * f[0], max32(&s[32]) * f[1]),
+                       fmaxf(max32(&s[64]) * f[2], max32(&s[96]) * f[3]));
       }
       const bool need = m_cand > m_used + kTau;
       // a row whose tile maximum passed its reference by more than kTau moves the
@@ -304,10 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float p0 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 0]), f[blk], -off));
-          float p1 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 1]), f[blk], -off));
-          float p2 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 2]), f[blk], -off));
-          float p3 = ex2_approx(fmaf(u2f(s[32 * blk + 4 * e + 3]), f[blk], -off));
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, u2f(s[32 * blk + 4 * e + 0]), u2f(s[32 * blk + 4 * e + 1]), f[blk], f[blk], -off, -off);
+          ffma2(x2, x3, u2f(s[32 * blk + 4 * e + 2]), u2f(s[32 * blk + 4 * e + 3]), f[blk], f[blk], -off, -off);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
+          float p2 = ex2_approx(x2);
+          float p3 = ex2_approx(x3);
           if (valid < kBN) {
             // keys past S: probability 0 (their scale may be 0, and 0 * -inf is NaN)
             const int c0 = 32 * blk + 4 * e;
@@ -316,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             p2 = c0 + 2 < valid ? p2 : 0.0f;
             p3 = c0 + 3 < valid ? p3 : 0.0f;
           }
-          rs0 += p0 + p1;
-          rs1 += p2 + p3;
+          fadd2(rs0, rs1, rs0, rs1, p0, p1);
+          fadd2(rs0, rs1, rs0, rs1, p2, p3);
           pk[e] = pack_e4m3x4(p0, p1, p2, p3);
         }
         tmem_st8(tS + 8 * blk, pk);
@@ -325,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (blk == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
             // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
             // before the first half of P_j V_j accumulates into it
-            if (mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+            if (mbar_wait_warp<true>(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
               tc_fence_after();
 #pragma unroll
               for (int c2 = 0; c2 < 8; ++c2) {
@@ -349,9 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       l += rs0 + rs1;
+
     }
 
-    if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+    if (ok && n > 0 && mbar_wait_warp<true>(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* vs = p.v_scale + (long long)bh * 128;
