@@ -37,6 +37,22 @@ METRIC = "attention TFLOPS (4·B·H·S²·D/s) at S=76112,H=40,D=128; % of tenso
 KERNELS_PER_STEP = 5  # attn_bf16, prep_qk_vmax, prep_v, widen_i8_f16, sage_attn
 
 
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken (or no summary)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    if workload != "wan720p" or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    srcs = ["sage_attention_forward_gb300/csrc/ptx.cuh", f"sage_attention_forward_gb300/csrc/{kernel}.cu"]
+    h = hashlib.sha256(b"".join(open(os.path.join(ROOT, p), "rb").read() for p in srcs)).hexdigest()
+    if h != rec.get("kernel_source_sha256"):
+        return None
+    return rec["dram_bytes_per_launch_wan720p_scaled"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -214,7 +230,8 @@ def run_ours(args, rank, world):
         "providers": providers,
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": bf16_tflops,
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": bf16_tflops / peaks["bf16_sustained"], "traffic": None,
+                     "frac": bf16_tflops / peaks["bf16_sustained"],
+                     "traffic": kernel_traffic("attn_bf16", wl.name),
                      "peak_source": f"{peaks['source']} bf16 sustained"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": e2e,
