@@ -137,6 +137,35 @@ ATTN_API attn_status sage_prepare(const void* q, const void* k, const void* v, i
                          void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * sage_prepare_noalloc -- sage_prepare without a workspace argument.  None of the
+ * pages has a counterpart; it exists for callers that cannot allocate device
+ * memory when they call us: code whose device memory is owned and budgeted by
+ * a host framework or engine, code that must not risk an out-of-memory failure
+ * or the device-wide synchronisation cudaMalloc/cudaFree can cause in the middle
+ * of a step, and plug-ins that are handed input and output buffers only.
+ *   Arguments, layouts, results and errors are those of sage_prepare (the outputs
+ *   are bit-identical); the scratch it needs (the per-channel maxima of |V|) is a
+ *   1 MiB array inside this library instead:
+ *   - limit: B * H <= 2048 heads; larger calls return ATTN_ERR_INVALID_ARG without
+ *     launching anything (use sage_prepare for them);
+ *   - the array lives on every device that loads the library, until the process
+ *     exits; this function never calls cudaMalloc, cudaFree or any allocating
+ *     routine;
+ *   - its first call on a device looks the array's device address up (a driver
+ *     query, once per device); make that first call before capturing a stream;
+ *   - all calls on a device share the array: the call clears it on `stream`
+ *     before use, so what an earlier call left does not matter, but two calls
+ *     whose work can overlap on the GPU (different streams without ordering)
+ *     race on it -- order them.
+ */
+ATTN_API attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                          const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                          float softmax_scale, const void* q_norm_w, const void* k_norm_w,
+                                          float rms_eps, const void* rope_cos, const void* rope_sin, int rope_dim,
+                                          int64_t S_pad, int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8,
+                                          float* q_scale, float* k_scale, float* v_scale, attn_stream_t stream);
+
+/*
  * sage_attn_workspace_size -- bytes of device scratch sage_attn_fwd needs:
  * the INT8 Q and K codes widened to FP16, 2 * 2 * B * H * S_pad * 128 bytes.
  * (sm_103a has no INT8 tensor-core MMA; the codes are widened exactly and the

@@ -23,7 +23,8 @@ import torch
 
 from .build import LIB as _LIB_PATH
 
-__all__ = ["AttnError", "attn_fwd_bf16", "sage_prepare", "sage_attn_fwd", "sage_attention", "Prepared",
+__all__ = ["AttnError", "attn_fwd_bf16", "sage_prepare", "sage_prepare_noalloc", "sage_attn_fwd", "sage_attention",
+           "Prepared",
            "sage_padded_len", "attn_get_device_status", "lib", "STATUS"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_ALIGNMENT", 3: "ATTN_ERR_UNSUPPORTED",
@@ -61,6 +62,10 @@ def lib() -> ctypes.CDLL:
                                    ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    ctypes.c_size_t, _vp]
         L.sage_prepare.restype = i
+        L.sage_prepare_noalloc.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp,
+                                           _vp, ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp]
+        L.sage_prepare_noalloc.restype = i
         L.sage_attn_workspace_size.argtypes = [i, i, ctypes.c_int64]
         L.sage_attn_workspace_size.restype = ctypes.c_size_t
         L.sage_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _I64x3, i, i, i, i, ctypes.c_int64, _vp,
@@ -173,6 +178,36 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
                               ptr(rope_sin), int(rope_dim), int(S_pad), out.q_i8.data_ptr(), out.k_i8.data_ptr(),
                               out.v_fp8.data_ptr(), out.q_scale.data_ptr(), out.k_scale.data_ptr(),
                               out.v_scale.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+    return out
+
+
+def sage_prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: Prepared,
+                         softmax_scale: float | None = None, q_norm_w: torch.Tensor | None = None,
+                         k_norm_w: torch.Tensor | None = None, rms_eps: float = 1e-6,
+                         rope_cos: torch.Tensor | None = None, rope_sin: torch.Tensor | None = None,
+                         rope_dim: int = 0, stream=None) -> Prepared:
+    """sage_prepare for callers that cannot allocate device memory at call time.
+
+    The library call allocates nothing: the caller passes every output buffer
+    (`out`, e.g. from Prepared.empty at set-up time) and the scratch comes from a
+    fixed 1 MiB array inside the library, so B * H is limited to 2048 heads.
+    Calls on one device share that array: order calls that could overlap on the
+    GPU, and make the first call on a device before capturing a stream.
+    """
+    B, S, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    qs, ks, vs = _bshd("q", q), _bshd("k", k), _bshd("v", v)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    _check(lib().sage_prepare_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
+                                      float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps),
+                                      ptr(rope_cos), ptr(rope_sin), int(rope_dim), int(out.S_pad),
+                                      out.q_i8.data_ptr(), out.k_i8.data_ptr(), out.v_fp8.data_ptr(),
+                                      out.q_scale.data_ptr(), out.k_scale.data_ptr(), out.v_scale.data_ptr(),
+                                      _stream_ptr(stream)))
     return out
 
 

@@ -199,6 +199,78 @@ attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, 
   return ATTN_OK;
 }
 
+attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                 const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                 float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                 const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                 int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
+                                 float* v_scale, attn_stream_t stream) {
+  TRY(check_shape(B, S, H, D));
+  if ((long long)B * H > sa::kNoAllocMaxHeads)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "sage_prepare_noalloc: B*H=%lld heads exceeds the %d heads its static scratch holds; use "
+                "sage_prepare with a caller-allocated workspace",
+                (long long)B * H, sa::kNoAllocMaxHeads);
+  sa::PrepareArgs a;
+  TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
+  TRY(check_strides("k", k, k_str, B, S, H, a.str[1]));
+  TRY(check_strides("v", v, v_str, B, S, H, a.str[2]));
+  if (!std::isfinite(softmax_scale)) return fail(ATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (S_pad < S || S_pad % 128 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
+  if (S_pad / 32 > (1ll << 30)) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
+    return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
+  if (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w)))
+    return fail(ATTN_ERR_ALIGNMENT, "RMSNorm weights must be 16-byte aligned");
+  if (q_norm_w && !(rms_eps >= 0.0f && std::isfinite(rms_eps)))
+    return fail(ATTN_ERR_INVALID_ARG, "rms_eps must be finite and >= 0");
+  if (!(rope_dim == 0 || rope_dim == 32 || rope_dim == 64 || rope_dim == 96 || rope_dim == 128))
+    return fail(ATTN_ERR_INVALID_ARG, "rope_dim=%d must be one of 0, 32, 64, 96, 128", rope_dim);
+  if (rope_dim > 0) {
+    if (!rope_cos || !rope_sin) return fail(ATTN_ERR_INVALID_ARG, "rope_dim > 0 needs rope_cos and rope_sin");
+    if (!aligned16(rope_cos) || !aligned16(rope_sin))
+      return fail(ATTN_ERR_ALIGNMENT, "RoPE tables must be 16-byte aligned");
+  }
+  struct {
+    const char* n;
+    const void* p;
+  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8},
+              {"q_scale", q_scale}, {"k_scale", k_scale}, {"v_scale", v_scale}};
+  for (auto& t : outs) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  TRY(check_device());
+  uint32_t* scratch = nullptr;
+  cudaError_t e = sa::noalloc_prepare_scratch(&scratch);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc: looking up the static scratch");
+  a.x[0] = q;
+  a.x[1] = k;
+  a.x[2] = v;
+  a.B = B;
+  a.S = S;
+  a.H = H;
+  a.S_pad = S_pad;
+  a.q_norm_w = q_norm_w;
+  a.k_norm_w = k_norm_w;
+  a.rms_eps = rms_eps;
+  a.rope_cos = rope_dim > 0 ? rope_cos : nullptr;
+  a.rope_sin = rope_dim > 0 ? rope_sin : nullptr;
+  a.rope_dim = rope_dim;
+  a.q_i8 = q_i8;
+  a.k_i8 = k_i8;
+  a.v_fp8 = v_fp8;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.c_log2 = (float)((double)softmax_scale * kLog2e);
+  a.vmax = scratch;  // zeroed on the stream by the launcher before the kernels use it
+  e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc launch");
+  return ATTN_OK;
+}
+
 int64_t sage_padded_len(int64_t S) { return S <= 0 ? 0 : ((S + 127) / 128) * 128; }
 
 size_t sage_prepare_workspace_size(int B, int H) {

@@ -41,6 +41,11 @@ struct PrepareArgs {
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 
+// Device address (current device) of the static scratch used by the
+// allocation-free prepare entry point; it holds kNoAllocMaxHeads * 128 words.
+constexpr int kNoAllocMaxHeads = 2048;
+cudaError_t noalloc_prepare_scratch(uint32_t** out);
+
 // Sage attention on prepared tensors (sage_attn.cu)
 size_t sage_attn_smem_bytes();
 cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,

@@ -20,6 +20,8 @@
 // writes with 128-bit stores into the [B, H, 128, S_pad] layout.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -305,7 +307,33 @@ __global__ void __launch_bounds__(128) prep_v_kernel(const VParams p) {
     *reinterpret_cast<uint4*>(out + (long long)k * p.S_pad) = make_uint4(col[k][0], col[k][1], col[k][2], col[k][3]);
 }
 
+// Scratch of the allocation-free prepare entry point: the per-(b, h, channel)
+// maxima of |V| for up to kNoAllocMaxHeads heads (B * H), 1 MiB in total.  It
+// is a plain device global: every GPU that loads this library holds it until
+// the process exits, and every call of that entry point on a device shares it.
+__device__ __align__(256) static uint32_t g_prepare_scratch[kNoAllocMaxHeads * 128];
+
 }  // namespace
+
+cudaError_t noalloc_prepare_scratch(uint32_t** out) {
+  // In host code g_prepare_scratch only names the symbol; its device address is
+  // looked up once per device, with that device current, and cached.
+  static std::mutex mu;
+  static uint32_t* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_prepare_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
 
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   const int nblk = (int)(a.S_pad / 32);
