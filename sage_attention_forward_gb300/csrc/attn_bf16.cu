@@ -14,12 +14,18 @@
 //   warp 8      TMA producer: Q tiles once, then K_j, V_j into a 4-slot ring
 //   warp 9      MMA issuer:   S_i = Q_i K_j^T and O_i += P_i V_j on tcgen05
 //                             (kind::f16, FP32 accumulators in TMEM)
-//   warps 0-3   softmax for Q tile 0, one thread per row (TMEM lanes 0-127)
-//   warps 4-7   softmax for Q tile 1
+//   warps 0-7   softmax: warps 0-3 own key columns [0,64) and warps 4-7 key
+//               columns [64,128) of every score tile (one thread per row and
+//               half-row, TMEM lane = row); both warpgroups take Q tile 0 then
+//               Q tile 1 each step and exchange half-row maxima in shared memory
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (BF16, two per column) overwrites the first 64 columns of S_i and is
-// the A operand of the PV MMA straight from TMEM.  The two Q tiles ping-pong:
-// while one warpgroup exponentiates S_0, the tensor core runs S_1 and P V.
+// the A operand of the PV MMA straight from TMEM, each warpgroup writing the
+// half of P for its key columns.  The two Q tiles ping-pong: while the softmax
+// warps exponentiate S_0, the tensor core runs S_1 and P V.  Splitting each
+// tile's columns over both warpgroups halves the time from a tile's scores to
+// its P, which is the chain that bounds the kernel (scores done -> softmax ->
+// P V -> next scores of that tile).
 // Rescaling is lazy: the reference maximum of a row moves only when a tile's
 // maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau and O
 // is rescaled rarely; the final division uses the same reference, so the
@@ -52,7 +58,10 @@ struct __align__(1024) Smem {
   uint64_t s_full[kNQ];
   uint64_t p_full[kNQ][2];   // P_i keys [0,64) and [64,128) stored in TMEM
   uint64_t o_done[kNQ];
-  uint64_t turn[kNQ];        // softmax turn token: the two Q tiles' softmax sections alternate
+  uint64_t xch[kNQ];         // half-row maxima of Q tile i exchanged (all 8 softmax warps)
+  uint64_t xfin[kNQ];        // half-row sums of Q tile i exchanged (epilogue)
+  float xmax[kNQ][2][kBM];   // half-row maxima, [tile][column half][row]
+  float xsum[kNQ][2][kBM];   // half-row sums
   uint64_t mma_drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -94,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i][0], 4);
       mbar_init(&sm.p_full[i][1], 4);
       mbar_init(&sm.o_done[i], 1);
-      mbar_init(&sm.turn[i], 4);
+      mbar_init(&sm.xch[i], 8);
+      mbar_init(&sm.xfin[i], 8);
     }
     mbar_init(&sm.mma_drain, 1);
     sm.abort_flag = 0;
@@ -225,125 +235,133 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int i = warp >> 2;                 // which Q tile
+    const int hb = warp >> 2;                // key-column half [64hb, 64hb + 64) of every tile
     const int wq = warp & 3;                 // TMEM lane quarter of this warp
-    const int row = wq * 32 + lane;          // row inside the Q tile
+    const int row = wq * 32 + lane;          // row inside a Q tile
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + 128u * i;
-    const uint32_t tO = tmem + lane_off + 256u + 128u * i;
     const float c = p.c_log2;
     uint32_t* err = &g_err_bf16;
-    float m_used = -INFINITY, l = 0.0f;
+    float m_used[kNQ] = {-INFINITY, -INFINITY};
+    float l[kNQ] = {0.0f, 0.0f};             // this thread's half of the row sums
     bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      if (!mbar_wait_warp(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
-      // the two Q tiles' softmax sections alternate (tile 0 of step j, tile 1 of step
-      // j, tile 0 of step j+1, ...), so each runs its exponentials without sharing the
-      // SM sub-partitions' MUFU and issue slots with the other
-      if ((i == 1 || j > 0) &&
-          !mbar_wait_warp(&sm.turn[i], (i == 0 ? j - 1 : j) & 1, abort_flag, err, kErrTimeoutSync)) {
+    for (int j = 0; j < n && ok; ++j) {
+#pragma unroll
+      for (int i = 0; i < kNQ; ++i) {
+        const uint32_t tS = tmem + lane_off + 128u * i + 64u * hb;
+        const uint32_t tO = tmem + lane_off + 256u + 128u * i + 64u * hb;
+        if (!mbar_wait_warp(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[64];
+        uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+        uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+        tmem_ld32(tS + 0, s0);
+        tmem_ld32(tS + 32, s1);
+        tmem_ld_wait();
+        tmem_reg_fence(s0);
+        tmem_reg_fence(s1);
+        const int valid = p.S - j * kBN - 64 * hb;   // valid keys in this half (may be <= 0)
+        if (valid < 64) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e >= valid) s[e] = f2u(-INFINITY);
+        }
+        // the row maximum over both halves: publish this half's, read the other's
+        const float lm = fmaxf(max32(&s[0]), max32(&s[32]));
+        sm.xmax[i][hb][row] = lm;
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.xch[i]);
+        if (!mbar_wait_warp(&sm.xch[i], j & 1, abort_flag, err, kErrTimeoutSync)) {
+          ok = false;
+          break;
+        }
+        const float m_cand = fmaxf(lm, sm.xmax[i][hb ^ 1][row]) * c;
+        // a row whose tile maximum passed its reference by more than kTau moves the
+        // reference (both halves of the row decide alike); O and l are brought to
+        // the new reference by the factor sc
+        const bool need = m_cand > m_used[i] + kTau;
+        const float sc = need ? ex2_approx(m_used[i] - m_cand) : 1.0f;
+        if (need) {
+          l[i] *= sc;
+          m_used[i] = m_cand;
+        }
+        const float neg_m = -m_used[i];
+        float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          // 32 scores -> 16 packed BF16 pairs: P columns [32hb + 16cc, 32hb + 16cc + 16)
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            ffma2(x0, x1, u2f(s[32 * cc + 2 * e]), u2f(s[32 * cc + 2 * e + 1]), c, c, neg_m, neg_m);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            fadd2(rs0, rs1, rs0, rs1, p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tmem + lane_off + 128u * i + 32u * hb + 16u * cc, pk);
+        }
+        l[i] += rs0 + rs1;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O_i must hold P_{j-1} V_{j-1} before this half of its columns is rescaled,
+          // and be rescaled before P_j V_j accumulates into it
+          if (!mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+            tmem_st_wait();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {
+            uint32_t o[16];
+            tmem_ld16(tO + 16 * c2, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
+            tmem_st16(tO + 16 * c2, o);
+          }
+        }
+        // this warpgroup's half of P_i is in TMEM: the P V MMA on those keys may start
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[i][hb]);
+      }
+    }
+
+    // epilogue: both halves' row sums, then this half of O's columns
+#pragma unroll
+    for (int i = 0; i < kNQ; ++i) {
+      if (!ok || n == 0) break;
+      if (!mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t s[128];
-      uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-      uint32_t(&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-      uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
-      uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-      const int valid = p.S - j * kBN;
-      float mx;
-      tmem_ld32(tS + 0, s0);
-      tmem_ld32(tS + 32, s1);
-      tmem_ld_wait();
-      tmem_reg_fence(s0);
-      tmem_reg_fence(s1);
-      tmem_ld32(tS + 64, s2);
-      tmem_ld32(tS + 96, s3);
-      if (valid >= kBN) {
-        // the first half's maximum overlaps the second half's load
-        const float mx01 = fmaxf(max32(&s[0]), max32(&s[32]));
-        tmem_ld_wait();
-        tmem_reg_fence(s2);
-        tmem_reg_fence(s3);
-        mx = fmaxf(mx01, fmaxf(max32(&s[64]), max32(&s[96])));
-      } else {
-        tmem_ld_wait();
-        tmem_reg_fence(s2);
-        tmem_reg_fence(s3);
-#pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (e >= valid) s[e] = f2u(-INFINITY);
-        mx = fmaxf(fmaxf(max32(&s[0]), max32(&s[32])), fmaxf(max32(&s[64]), max32(&s[96])));
+      sm.xsum[i][hb][row] = l[i];
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.xfin[i]);
+      if (!mbar_wait_warp(&sm.xfin[i], 0, abort_flag, err, kErrTimeoutSync)) {
+        ok = false;
+        break;
       }
-      const float m_cand = mx * c;
-      const bool need = m_cand > m_used + kTau;
-      // a row whose tile maximum passed its reference by more than kTau moves the
-      // reference; O and l are brought to the new reference by the factor sc
-      const float sc = need ? ex2_approx(m_used - m_cand) : 1.0f;
-      if (need) {
-        l *= sc;
-        m_used = m_cand;
-      }
-      const float neg_m = -m_used;
-      float rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        // 32 scores -> 16 packed BF16 pairs, stored as P columns [16cc, 16cc + 16)
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x0, x1;
-          ffma2(x0, x1, u2f(s[32 * cc + 2 * e]), u2f(s[32 * cc + 2 * e + 1]), c, c, neg_m, neg_m);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          fadd2(rs0, rs1, rs0, rs1, p0, p1);
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + 16 * cc, pk);
-        if (cc & 1) {
-          if (cc == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
-            // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
-            // before the first half of P_j V_j accumulates into it
-            if (mbar_wait_warp(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
-              tc_fence_after();
-#pragma unroll
-              for (int c2 = 0; c2 < 8; ++c2) {
-                uint32_t o[16];
-                tmem_ld16(tO + 16 * c2, o);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
-                tmem_st16(tO + 16 * c2, o);
-              }
-            } else {
-              ok = false;
-            }
-          }
-          // keys [0,64) then [64,128) of P_i are ready: the PV MMA on them may start
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (ok && lane == 0) mbar_arrive(&sm.p_full[i][cc >> 1]);
-        }
-      }
-      if (!ok) break;
-      l += rs0 + rs1;
-      // hand the turn to the other Q tile's softmax
-      if (lane == 0) mbar_arrive(&sm.turn[i ^ 1]);
-    }
-
-    if (ok && n > 0 && mbar_wait_warp(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / (l[i] + sm.xsum[i][hb ^ 1][row]);
       const int grow = q_row0 + i * kBM + row;
-      __nv_bfloat16* dst = p.o + (long long)b * p.o_sb + (long long)grow * p.o_ss + (long long)h * p.o_sh;
+      const uint32_t tO = tmem + lane_off + 256u + 128u * i + 64u * hb;
+      __nv_bfloat16* dst =
+          p.o + (long long)b * p.o_sb + (long long)grow * p.o_ss + (long long)h * p.o_sh + 64 * hb;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * cc, o);
         tmem_ld_wait();
+        tmem_reg_fence(o);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l);
