@@ -28,9 +28,12 @@
 // (e4m3) overwrites the first 32 columns of S_i.  The reference maximum moves
 // only when a tile's maximum exceeds it by more than kTau (log2 units).
 // Unlike the BF16 kernel, the two softmax warpgroups are not made to take
-// turns, and every wait sleeps on its barrier: with the cheaper e4m3 P V
-// product the softmax warps are the busiest units, and overlapping the two
-// warpgroups' sections keeps the SM sub-partitions' issue slots fuller.
+// turns: with the cheaper e4m3 P V product the softmax warps are the busiest
+// units, and overlapping the two warpgroups' sections keeps the SM
+// sub-partitions' issue slots fuller.  The waits on the critical hand-offs
+// (the MMA warp's, and a softmax warpgroup's wait for its S tile) poll; the
+// producer's and the O-rescale waits sleep on their barriers, which gives
+// their issue slots to the softmax warps.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int i, int slot, int j) -> bool {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait_warp<true>(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
+          if (!mbar_wait_warp<false>(&sm.p_full[i][half], j & 1, abort_flag, err, kErrTimeoutSync)) return false;
           tc_fence_after();
           issue_pv_half(i, slot, half, j > 0);
         }
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
-      bool ok = mbar_wait_warp<true>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
-      if (ok) ok = mbar_wait_warp<true>(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
+      bool ok = mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) ok = mbar_wait_warp<false>(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -229,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slotV = j % kVStages;
         const int slotK = (j + 1) % kKStages;
         const bool more = (j + 1 < n);
-        if (!mbar_wait_warp<true>(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+        if (!mbar_wait_warp<false>(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
         if (!issue_pv(0, slotV, j)) break;
         if (more) {
-          if (!mbar_wait_warp<true>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
+          if (!mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
           tc_fence_after();
           issue_s(0, slotK);
           if (leader) mma_commit(&sm.s_full[0]);
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 ks4 = ks_next;
       if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
       const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
-      if (!mbar_wait_warp<true>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
+      if (!mbar_wait_warp<false>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
       tc_fence_after();
       uint32_t s[128];
       uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
