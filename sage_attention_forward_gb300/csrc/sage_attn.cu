@@ -37,6 +37,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -319,58 +321,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float off = m_used + kTau - kLog2_448;
       float rs0 = 0.0f, rs1 = 0.0f;
+      // the key mask only exists in the tile that holds the ragged tail, so the loop is
+      // compiled twice rather than carrying 128 predicated selects through every tile
+      auto p_section = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        // 32 scores of key block blk -> 8 words of four e4m3 each, P columns [8blk, 8blk + 8)
-        uint32_t pk[8];
+        for (int blk = 0; blk < 4; ++blk) {
+          // 32 scores of key block blk -> 8 words of four e4m3 each, P columns [8blk, 8blk + 8)
+          uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float x0, x1, x2, x3;
-          ffma2(x0, x1, u2f(s[32 * blk + 4 * e + 0]), u2f(s[32 * blk + 4 * e + 1]), f[blk], f[blk], -off, -off);
-          ffma2(x2, x3, u2f(s[32 * blk + 4 * e + 2]), u2f(s[32 * blk + 4 * e + 3]), f[blk], f[blk], -off, -off);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          float p2 = ex2_approx(x2);
-          float p3 = ex2_approx(x3);
-          if (valid < kBN) {
-            // keys past S: probability 0 (their scale may be 0, and 0 * -inf is NaN)
-            const int c0 = 32 * blk + 4 * e;
-            p0 = c0 + 0 < valid ? p0 : 0.0f;
-            p1 = c0 + 1 < valid ? p1 : 0.0f;
-            p2 = c0 + 2 < valid ? p2 : 0.0f;
-            p3 = c0 + 3 < valid ? p3 : 0.0f;
-          }
-          fadd2(rs0, rs1, rs0, rs1, p0, p1);
-          fadd2(rs0, rs1, rs0, rs1, p2, p3);
-          pk[e] = pack_e4m3x4(p0, p1, p2, p3);
-        }
-        tmem_st8(tS + 8 * blk, pk);
-        if (blk & 1) {
-          if (blk == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
-            // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
-            // before the first half of P_j V_j accumulates into it
-            if (mbar_wait_warp<true>(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
-              tc_fence_after();
-#pragma unroll
-              for (int c2 = 0; c2 < 8; ++c2) {
-                uint32_t o[16];
-                tmem_ld16(tO + 16 * c2, o);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
-                tmem_st16(tO + 16 * c2, o);
-              }
-            } else {
-              ok = false;
+          for (int e = 0; e < 8; ++e) {
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, u2f(s[32 * blk + 4 * e + 0]), u2f(s[32 * blk + 4 * e + 1]), f[blk], f[blk], -off, -off);
+            ffma2(x2, x3, u2f(s[32 * blk + 4 * e + 2]), u2f(s[32 * blk + 4 * e + 3]), f[blk], f[blk], -off, -off);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            float p2 = ex2_approx(x2);
+            float p3 = ex2_approx(x3);
+            if (kMasked) {
+              // keys past S: probability 0 (their scale may be 0, and 0 * -inf is NaN)
+              const int c0 = 32 * blk + 4 * e;
+              p0 = c0 + 0 < valid ? p0 : 0.0f;
+              p1 = c0 + 1 < valid ? p1 : 0.0f;
+              p2 = c0 + 2 < valid ? p2 : 0.0f;
+              p3 = c0 + 3 < valid ? p3 : 0.0f;
             }
+            fadd2(rs0, rs1, rs0, rs1, p0, p1);
+            fadd2(rs0, rs1, rs0, rs1, p2, p3);
+            pk[e] = pack_e4m3x4(p0, p1, p2, p3);
           }
-          // keys [0,64) then [64,128) of P_i are ready: the PV MMA on them may start
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (ok && lane == 0) mbar_arrive(&sm.p_full[i][blk >> 1]);
+          tmem_st8(tS + 8 * blk, pk);
+          if (blk & 1) {
+            if (blk == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
+              // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
+              // before the first half of P_j V_j accumulates into it
+              if (mbar_wait_warp<true>(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c2 = 0; c2 < 8; ++c2) {
+                  uint32_t o[16];
+                  tmem_ld16(tO + 16 * c2, o);
+                  tmem_ld_wait();
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
+                  tmem_st16(tO + 16 * c2, o);
+                }
+              } else {
+                ok = false;
+              }
+            }
+            // keys [0,64) then [64,128) of P_i are ready: the PV MMA on them may start
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&sm.p_full[i][blk >> 1]);
+          }
         }
-      }
+      };
+      if (valid < kBN) p_section(std::true_type{});
+      else p_section(std::false_type{});
       if (!ok) break;
       l += rs0 + rs1;
 
