@@ -18,6 +18,10 @@ Functions and the passages they follow:
   quant_qk       -- Q/K to INT8, one FP32 scale per (batch, head, 32-row
                     block), Q's scale carrying softmax_scale*log2(e) (same
                     pull request, Technical Details).
+  k_mean         -- K smoothing: the per-(batch, head, channel) mean of K over
+                    its tokens, subtracted before quantising K (ai-infra
+                    handbook chapter above, section "SageAttention:
+                    quantizing attention too").
   quant_v        -- V to FP8 e4m3 transposed to [B, H, 128, S_pad], one FP32
                     scale per channel (same pull request, Technical Details).
   prepare        -- the three above in order, as the prepare stage runs them.
@@ -54,7 +58,8 @@ def lib():
         L.oracle_norm_rope.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, c_p, ctypes.c_float,
                                        c_p, c_p, ctypes.c_int, c_p]
         L.oracle_quant_qk.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                      ctypes.c_float, c_p, c_p]
+                                      ctypes.c_float, c_p, c_p, c_p]
+        L.oracle_k_mean.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, c_p]
         L.oracle_quant_v.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, c_p, c_p]
         L.oracle_e4m3_encode_array.argtypes = [c_p, c_p, ctypes.c_int64]
         L.oracle_e4m3_decode_array.argtypes = [c_p, c_p, ctypes.c_int64]
@@ -125,14 +130,30 @@ def norm_rope(x: torch.Tensor, norm_w: torch.Tensor | None, eps: float,
     return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16).reshape(B, S, H, D)
 
 
-def quant_qk(x: torch.Tensor, S_pad: int, scale_mult: float = 1.0):
-    """INT8 codes [B, H, S_pad, 128] and FP32 scales [B, H, S_pad/32]."""
+def quant_qk(x: torch.Tensor, S_pad: int, scale_mult: float = 1.0, mean: torch.Tensor | None = None):
+    """INT8 codes [B, H, S_pad, 128] and FP32 scales [B, H, S_pad/32]; with
+    `mean` ([B, H, 128] float32) the value quantised is fl32(x - mean)."""
     B, S, H, D = x.shape
     xb = _bf16_bits(x)
     codes = np.empty((B, H, S_pad, 128), dtype=np.int8)
     scales = np.empty((B, H, S_pad // 32), dtype=np.float32)
-    lib().oracle_quant_qk(_ptr(xb), B, S, H, int(S_pad), float(np.float32(scale_mult)), _ptr(codes), _ptr(scales))
+    mb = None
+    if mean is not None:
+        mb = np.ascontiguousarray(mean.to(torch.float32).numpy())
+        assert mb.shape == (B, H, 128)
+    lib().oracle_quant_qk(_ptr(xb), B, S, H, int(S_pad), float(np.float32(scale_mult)),
+                          _ptr(mb) if mb is not None else None, _ptr(codes), _ptr(scales))
     return torch.from_numpy(codes), torch.from_numpy(scales)
+
+
+def k_mean(x: torch.Tensor, S_pad: int) -> torch.Tensor:
+    """Per-(batch, head, channel) mean of K over its S tokens, float32 [B, H, 128],
+    summed in the order oracle.c documents (K smoothing)."""
+    B, S, H, D = x.shape
+    xb = _bf16_bits(x)
+    out = np.empty((B, H, 128), dtype=np.float32)
+    lib().oracle_k_mean(_ptr(xb), B, S, H, int(S_pad), _ptr(out))
+    return torch.from_numpy(out)
 
 
 def quant_v(x: torch.Tensor, S_pad: int):
@@ -151,11 +172,13 @@ def padded_len(S: int) -> int:
 
 
 def prepare(q, k, v, softmax_scale, S_pad=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6,
-            rope_cos=None, rope_sin=None, rope_dim=0):
-    """The Sage prepare stage: optional norm/RoPE of Q and K, then the quantisers.
+            rope_cos=None, rope_sin=None, rope_dim=0, smooth_k=False):
+    """The Sage prepare stage: optional norm/RoPE of Q and K, optional K
+    smoothing (subtract k_mean before quantising K), then the quantisers.
 
-    Returns a dict with q_i8, k_i8, v_fp8 (uint8), q_scale, k_scale, v_scale and
-    the BF16 Q/K that were quantised (q_pre, k_pre).
+    Returns a dict with q_i8, k_i8, v_fp8 (uint8), q_scale, k_scale, v_scale,
+    the BF16 Q/K that were quantised (q_pre, k_pre) and k_mean (None unless
+    smooth_k).
     """
     B, S, H, D = q.shape
     if S_pad is None:
@@ -166,10 +189,11 @@ def prepare(q, k, v, softmax_scale, S_pad=None, q_norm_w=None, k_norm_w=None, rm
         k_pre = norm_rope(k, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim)
     c = softmax_log2_factor(softmax_scale)
     q_i8, q_scale = quant_qk(q_pre, S_pad, c)
-    k_i8, k_scale = quant_qk(k_pre, S_pad, 1.0)
+    km = k_mean(k_pre, S_pad) if smooth_k else None
+    k_i8, k_scale = quant_qk(k_pre, S_pad, 1.0, km)
     v_fp8, v_scale = quant_v(v, S_pad)
     return dict(q_i8=q_i8, k_i8=k_i8, v_fp8=v_fp8, q_scale=q_scale, k_scale=k_scale, v_scale=v_scale,
-                q_pre=q_pre.contiguous(), k_pre=k_pre.contiguous(), S_pad=S_pad, log2_factor=c)
+                q_pre=q_pre.contiguous(), k_pre=k_pre.contiguous(), S_pad=S_pad, log2_factor=c, k_mean=km)
 
 
 def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool = False, p_e4m3: bool = False,

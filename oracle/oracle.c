@@ -274,11 +274,14 @@ void oracle_norm_rope(const uint16_t* x, int B, int S, int H, const uint16_t* w,
  *   scale = (a / 127) * scale_mult     for Q  (scale_mult = fl32(softmax_scale * log2 e))
  * a == 0 gives all-zero codes and scale 0.  The INT8 bytes therefore depend on
  * the tensor alone; the softmax factor lives in Q's scale.
+ * With `mean` given ([B, H, 128], K smoothing, see oracle_k_mean) the value
+ * quantised is fl32(x - mean[b, h, c]) in place of x, in both the block
+ * maximum and the codes.
  * Output layout [B, H, S_pad, 128] (row-major); rows in [S, S_pad) are zero and
  * the scales of blocks wholly beyond S are zero.  scales: [B, H, S_pad / 32].
  */
 void oracle_quant_qk(const uint16_t* x, int B, int S, int H, int64_t S_pad, float scale_mult,
-                     int8_t* codes, float* scales) {
+                     const float* mean, int8_t* codes, float* scales) {
     int64_t nblk = S_pad / 32;
 #pragma omp parallel for collapse(2) schedule(static)
     for (int b = 0; b < B; b++) {
@@ -286,9 +289,12 @@ void oracle_quant_qk(const uint16_t* x, int B, int S, int H, int64_t S_pad, floa
             for (int64_t j = 0; j < nblk; j++) {
                 int64_t r0 = 32 * j, r1 = r0 + 32 < S ? r0 + 32 : S;
                 float a = 0.0f;
+                const float* mu = mean ? mean + ((int64_t)b * H + h) * 128 : NULL;
                 for (int64_t s = r0; s < r1; s++)
                     for (int c = 0; c < 128; c++) {
-                        float xv = fabsf(oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]));
+                        float xv = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                        if (mu) xv = xv - mu[c];
+                        xv = fabsf(xv);
                         if (xv > a) a = xv;
                     }
                 float inv = (a > 0.0f) ? 127.0f / a : 0.0f;
@@ -297,6 +303,7 @@ void oracle_quant_qk(const uint16_t* x, int B, int S, int H, int64_t S_pad, floa
                     for (int c = 0; c < 128; c++) {
                         if (s >= S || a == 0.0f) { dst[c] = 0; continue; }
                         float xv = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                        if (mu) xv = xv - mu[c];
                         float t = xv * inv;
                         float rq = rintf(t);
                         if (rq > 127.0f) rq = 127.0f;
@@ -310,6 +317,52 @@ void oracle_quant_qk(const uint16_t* x, int B, int S, int H, int64_t S_pad, floa
                     sc = sc * scale_mult;
                 }
                 scales[((int64_t)b * H + h) * nblk + j] = sc;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------- Sage prepare: K smoothing */
+
+/*
+ * SageAttention smooths K before quantising it: it subtracts the mean of K,
+ * which takes out K's outlier channels (ai-infra handbook, "Kernel
+ * acceleration: attention, compilation and fusion", section "SageAttention:
+ * quantizing attention too").
+ *
+ * Reading: one mean per (batch, head, channel) over the S tokens of K (K after
+ * the optional RMSNorm + RoPE, i.e. the tensor that is quantised), subtracted
+ * before the INT8 quantisation (oracle_quant_qk with `mean`).  In exact
+ * arithmetic the attention output does not change: every score of a query row
+ * moves by the same q . mean, which the softmax cancels.
+ *
+ * The mean is a binary32 value that decides INT8 codes, so its summation
+ * order is fixed (a deterministic function of K; the CUDA prepare follows the
+ * same order).  For block j (rows 32j .. 32j+31, rows >= S skipped):
+ *   P_g = (((0 + x[32j+g]) + x[32j+4+g]) + ...) + x[32j+28+g]     g = 0..3
+ *   B_j = (P_0 + P_1) + (P_2 + P_3)
+ *   total = ((0 + B_0) + B_1) + ... + B_{nblk-1},   mean = total / S
+ * every + and the / in binary32, round to nearest even.
+ * x: [B, S, H, 128] BF16 bits; mean: [B, H, 128].
+ */
+void oracle_k_mean(const uint16_t* x, int B, int S, int H, int64_t S_pad, float* mean) {
+    int64_t nblk = S_pad / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < H; h++) {
+            for (int c = 0; c < 128; c++) {
+                float total = 0.0f;
+                for (int64_t j = 0; j < nblk; j++) {
+                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    for (int g = 0; g < 4; g++)
+                        for (int t = 0; t < 8; t++) {
+                            int64_t s = 32 * j + 4 * t + g;
+                            if (s < S) part[g] = part[g] + oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                        }
+                    float blk = (part[0] + part[1]) + (part[2] + part[3]);
+                    total = total + blk;
+                }
+                mean[((int64_t)b * H + h) * 128 + c] = total / (float)S;
             }
         }
     }
