@@ -137,6 +137,45 @@ ATTN_API attn_status sage_prepare(const void* q, const void* k, const void* v, i
                          void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * sage_prepare_smooth_k_workspace_size -- bytes of device scratch
+ * sage_prepare_smooth_k needs: the V maxima of sage_prepare plus one float per
+ * (b, h, 32-row block, channel) of block sums of K.
+ */
+ATTN_API size_t sage_prepare_smooth_k_workspace_size(int B, int H, int64_t S_pad);
+
+/*
+ * sage_prepare_smooth_k -- sage_prepare with K smoothing.  SageAttention
+ * subtracts the mean of K before quantising it, which removes K's outlier
+ * channels (ai-infra handbook, "Kernel acceleration: attention, compilation
+ * and fusion", section "SageAttention: quantizing attention too"); read here
+ * as one mean per (batch, head, channel) over the S tokens.  In exact
+ * arithmetic the attention output is unchanged: every score of a query row
+ * moves by the same q . k_mean, which the softmax cancels, so the result goes
+ * to sage_attn_fwd as it is.
+ *   All arguments as sage_prepare, plus
+ *   k_mean     : float [B, H, 128] output (caller-allocated, 16-byte aligned):
+ *                k_mean[b,h,c] = (sum over s < S of K'[b,s,h,c]) / S, K' being
+ *                K after the optional RMSNorm + RoPE.  The sum is taken in a
+ *                fixed binary32 order: per 32-row block j, four partial sums
+ *                P_g over rows 32j+4t+g (t = 0..7, ascending, from 0; rows >= S
+ *                skipped), B_j = (P_0 + P_1) + (P_2 + P_3), then the B_j added in
+ *                ascending j from 0, then divided by S.
+ *   k_i8, k_scale : as sage_prepare, of fl32(K' - k_mean[b,h,c]) in place of K'.
+ *   workspace  : at least sage_prepare_smooth_k_workspace_size(B, H, S_pad)
+ *                bytes, 16-byte aligned; its contents on entry do not matter.
+ * q_i8, q_scale, v_fp8 and v_scale are those of sage_prepare, bit for bit.
+ * Enqueues a memset and four kernels on `stream`.  Errors as sage_prepare;
+ * k_mean NULL -> ATTN_ERR_INVALID_ARG, misaligned -> ATTN_ERR_ALIGNMENT.
+ */
+ATTN_API attn_status sage_prepare_smooth_k(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                  const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                  float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                  const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                  int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
+                                  float* v_scale, float* k_mean, void* workspace, size_t workspace_bytes,
+                                  attn_stream_t stream);
+
+/*
  * sage_prepare_noalloc -- sage_prepare without a workspace argument.  None of the
  * pages has a counterpart; it exists for callers that cannot allocate device
  * memory when they call us: code whose device memory is owned and budgeted by

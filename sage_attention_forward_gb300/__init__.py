@@ -62,6 +62,12 @@ def lib() -> ctypes.CDLL:
                                    ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    ctypes.c_size_t, _vp]
         L.sage_prepare.restype = i
+        L.sage_prepare_smooth_k_workspace_size.argtypes = [i, i, ctypes.c_int64]
+        L.sage_prepare_smooth_k_workspace_size.restype = ctypes.c_size_t
+        L.sage_prepare_smooth_k.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp,
+                                            _vp, ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp,
+                                            _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.sage_prepare_smooth_k.restype = i
         L.sage_prepare_noalloc.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp,
                                            _vp, ctypes.c_float, _vp, _vp, i, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp]
@@ -134,6 +140,7 @@ class Prepared:
     v_scale: torch.Tensor   # fp32  [B, H, 128]
     S: int
     S_pad: int
+    k_mean: torch.Tensor | None = None   # fp32 [B, H, 128], set when K was smoothed
 
     @staticmethod
     def empty(B: int, H: int, S: int, S_pad: int, device) -> "Prepared":
@@ -145,8 +152,12 @@ class Prepared:
                         torch.empty((B, H, 128), dtype=torch.float32, device=device), S, S_pad)
 
 
-def prepare_workspace(B: int, H: int, device) -> torch.Tensor:
-    return torch.empty(int(lib().sage_prepare_workspace_size(B, H)), dtype=torch.uint8, device=device)
+def prepare_workspace(B: int, H: int, device, S_pad: int | None = None, smooth_k: bool = False) -> torch.Tensor:
+    if smooth_k:
+        n = int(lib().sage_prepare_smooth_k_workspace_size(B, H, int(S_pad)))
+    else:
+        n = int(lib().sage_prepare_workspace_size(B, H))
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def attn_workspace(B: int, H: int, S_pad: int, device) -> torch.Tensor:
@@ -157,8 +168,10 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
                  S_pad: int | None = None, q_norm_w: torch.Tensor | None = None,
                  k_norm_w: torch.Tensor | None = None, rms_eps: float = 1e-6, rope_cos: torch.Tensor | None = None,
                  rope_sin: torch.Tensor | None = None, rope_dim: int = 0, out: Prepared | None = None,
-                 workspace: torch.Tensor | None = None, stream=None) -> Prepared:
-    """Quantise Q/K to INT8 and V to e4m3 (optionally RMSNorm + RoPE on Q/K first)."""
+                 workspace: torch.Tensor | None = None, stream=None, smooth_k: bool = False) -> Prepared:
+    """Quantise Q/K to INT8 and V to e4m3 (optionally RMSNorm + RoPE on Q/K first;
+    with smooth_k, K's per-channel token mean is subtracted before quantising K
+    and returned in out.k_mean)."""
     B, S, H, D = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -167,12 +180,23 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
     if out is None:
         out = Prepared.empty(B, H, S, S_pad, q.device)
     if workspace is None:
-        workspace = prepare_workspace(B, H, q.device)
+        workspace = prepare_workspace(B, H, q.device, S_pad, smooth_k)
     qs, ks, vs = _bshd("q", q), _bshd("k", k), _bshd("v", v)
 
     def ptr(t):
         return None if t is None else t.data_ptr()
 
+    if smooth_k:
+        if out.k_mean is None:
+            out.k_mean = torch.empty((B, H, 128), dtype=torch.float32, device=q.device)
+        _check(lib().sage_prepare_smooth_k(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
+                                           float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps),
+                                           ptr(rope_cos), ptr(rope_sin), int(rope_dim), int(S_pad),
+                                           out.q_i8.data_ptr(), out.k_i8.data_ptr(), out.v_fp8.data_ptr(),
+                                           out.q_scale.data_ptr(), out.k_scale.data_ptr(), out.v_scale.data_ptr(),
+                                           out.k_mean.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                           _stream_ptr(stream)))
+        return out
     _check(lib().sage_prepare(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                               float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
                               ptr(rope_sin), int(rope_dim), int(S_pad), out.q_i8.data_ptr(), out.k_i8.data_ptr(),
@@ -229,10 +253,10 @@ def sage_attn_fwd(prep: Prepared, out: torch.Tensor | None = None, workspace: to
 
 
 def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
-                   rope_sin=None, rope_dim=0, out=None, stream=None) -> torch.Tensor:
+                   rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False) -> torch.Tensor:
     """Prepare + attention: the SageAttention-style forward of BF16 Q/K/V."""
     prep = sage_prepare(q, k, v, softmax_scale, None, q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim,
-                        stream=stream)
+                        stream=stream, smooth_k=smooth_k)
     return sage_attn_fwd(prep, out=out, stream=stream)
 
 

@@ -278,12 +278,13 @@ size_t sage_prepare_workspace_size(int B, int H) {
   return (size_t)B * (size_t)H * 128 * sizeof(uint32_t);
 }
 
-attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+static attn_status prepare_checked(const char* who, const void* q, const void* k, const void* v, int B, int S, int H, int D,
                          const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                          float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
                          const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
                          int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
-                         void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+                         void* workspace, size_t workspace_bytes, size_t workspace_needed, float* k_mean,
+                         attn_stream_t stream) {
   TRY(check_shape(B, S, H, D));
   sa::PrepareArgs a;
   TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
@@ -315,9 +316,9 @@ attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int
     if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
     if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
   }
-  if (workspace_bytes < sage_prepare_workspace_size(B, H))
-    return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
-                sage_prepare_workspace_size(B, H));
+  if (workspace_bytes < workspace_needed)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu required", who, workspace_bytes,
+                workspace_needed);
   TRY(check_device());
   a.x[0] = q;
   a.x[1] = k;
@@ -340,9 +341,47 @@ attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int
   a.v_scale = v_scale;
   a.c_log2 = (float)((double)softmax_scale * kLog2e);
   a.vmax = reinterpret_cast<uint32_t*>(workspace);
+  if (k_mean != nullptr) {
+    a.k_mean = k_mean;
+    // block sums after the V maxima, 16-byte aligned (B*H*128 words is a multiple of 4)
+    a.k_partial = reinterpret_cast<float*>(a.vmax + (size_t)B * H * 128);
+  }
   cudaError_t e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare launch");
+  if (e != cudaSuccess) return fail_cuda(e, who);
   return ATTN_OK;
+}
+
+attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                         const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                         float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                         const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
+                         int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
+                         void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  return prepare_checked("sage_prepare", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale, q_norm_w,
+                         k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8, q_scale,
+                         k_scale, v_scale, workspace, workspace_bytes, sage_prepare_workspace_size(B, H), nullptr,
+                         stream);
+}
+
+size_t sage_prepare_smooth_k_workspace_size(int B, int H, int64_t S_pad) {
+  if (B < 1 || H < 1 || S_pad < 1) return 0;
+  const size_t bh = (size_t)B * (size_t)H;
+  return bh * 128 * sizeof(uint32_t) + bh * (size_t)(S_pad / 32) * 128 * sizeof(float);
+}
+
+attn_status sage_prepare_smooth_k(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                  const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                  float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                  const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                  int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
+                                  float* v_scale, float* k_mean, void* workspace, size_t workspace_bytes,
+                                  attn_stream_t stream) {
+  if (k_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "sage_prepare_smooth_k: k_mean is NULL");
+  if (!aligned16(k_mean)) return fail(ATTN_ERR_ALIGNMENT, "sage_prepare_smooth_k: k_mean is not 16-byte aligned");
+  return prepare_checked("sage_prepare_smooth_k", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale,
+                         q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8,
+                         q_scale, k_scale, v_scale, workspace, workspace_bytes,
+                         sage_prepare_smooth_k_workspace_size(B, H, S_pad), k_mean, stream);
 }
 
 size_t sage_attn_workspace_size(int B, int H, int64_t S_pad) {

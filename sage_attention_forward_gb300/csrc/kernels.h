@@ -38,6 +38,8 @@ struct PrepareArgs {
   float* v_scale;
   float c_log2;
   uint32_t* vmax;            // workspace: B*H*128 words
+  float* k_mean = nullptr;   // K smoothing: output [B*H*128] (nullptr: no smoothing)
+  float* k_partial = nullptr;  // K smoothing workspace: [B*H, S_pad/32, 128] block sums
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 

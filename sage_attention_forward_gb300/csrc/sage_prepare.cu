@@ -14,6 +14,9 @@
 // registers while the block maximum is reduced.  For V the same warps only
 // take per-channel maxima, reduce them across the CTA and fold them into the
 // workspace with integer atomicMax on the (non-negative) float bits.
+// With K smoothing two kernels run first: per-block partial sums of K (same
+// warp layout) and one thread per (b, h, channel) adding them up into the
+// mean, which kernel 1 then subtracts from K.
 // Kernel 2 -- one CTA per (b, h, 128 positions): 128 threads, thread (c8, sg)
 // loads 16 positions x 8 channels, encodes them and transposes the bytes in
 // registers (byte permutes) into 8 rows of 16 consecutive positions, which it
@@ -43,6 +46,7 @@ struct QKParams {
   float* scales[2];
   float c_log2;                     // fl32(softmax_scale * log2 e), folded into Q's scales
   uint32_t* vmax;                   // [B*H*128] float bits of the channel maxima of |V|
+  const float* kmean;               // [B*H*128] K smoothing: subtracted from K before quantising (or nullptr)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -73,59 +77,18 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* src, uint32_t (&w)[8
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-__global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
-  const int task = blockIdx.z;
-  const int bh = blockIdx.y;
+// Rows 32*blk + 4*step + g (step = 0..7) of tensor `task` (0: Q, 1: K), channels
+// [16L, 16L + 16), after the optional RMSNorm and RoPE, as packed BF16 pairs;
+// rows >= S are zero.  Shared by the quantiser and the K-mean partial sums, so
+// both see the same bits.
+__device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, int blk, int lane,
+                                          uint32_t (&x)[8][8]) {
   const int b = bh / p.H, h = bh % p.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x * 8 + warp;
-  const int g = lane >> 3;   // row inside a 4-row step
-  const int L = lane & 7;    // channel group [16L, 16L+16)
+  const int g = lane >> 3;
+  const int L = lane & 7;
   const __nv_bfloat16* base = p.x[task] + (long long)b * p.sb[task] + (long long)h * p.sh[task] + 16 * L;
   const long long ss = p.ss[task];
-
-  if (task == 2) {
-    // -------------------------------------------------------- V channel maxima
-    __shared__ float red[8][128];
-    float mx[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) mx[k] = 0.0f;
-    if (blk < p.nblk) {
-#pragma unroll
-      for (int step = 0; step < 8; ++step) {
-        const int s = 32 * blk + 4 * step + g;
-        if (s < p.S) {
-          uint32_t w[8];
-          load16(base + (long long)s * ss, w);
-          float f[16];
-          unpack16(w, f);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], fabsf(f[k]));
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
-      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
-    }
-    if (g == 0) {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) red[warp][16 * L + k] = mx[k];
-    }
-    __syncthreads();
-    if (threadIdx.x < 128) {
-      float m = red[0][threadIdx.x];
-#pragma unroll
-      for (int w2 = 1; w2 < 8; ++w2) m = fmaxf(m, red[w2][threadIdx.x]);
-      if (m > 0.0f) atomicMax(&p.vmax[(long long)bh * 128 + threadIdx.x], __float_as_uint(m));
-    }
-    return;
-  }
-
-  if (blk >= p.nblk) return;
   // ---------------------------------------------------------- load 8 rows x 16 channels
-  uint32_t x[8][8];
 #pragma unroll
   for (int step = 0; step < 8; ++step) {
     const int s = 32 * blk + 4 * step + g;
@@ -197,6 +160,70 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
     }
   }
 
+}
+
+__global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
+  const int task = blockIdx.z;
+  const int bh = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x * 8 + warp;
+  const int g = lane >> 3;   // row inside a 4-row step
+  const int L = lane & 7;    // channel group [16L, 16L+16)
+  const __nv_bfloat16* base = p.x[task] + (long long)b * p.sb[task] + (long long)h * p.sh[task] + 16 * L;
+  const long long ss = p.ss[task];
+
+  if (task == 2) {
+    // -------------------------------------------------------- V channel maxima
+    __shared__ float red[8][128];
+    float mx[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) mx[k] = 0.0f;
+    if (blk < p.nblk) {
+#pragma unroll
+      for (int step = 0; step < 8; ++step) {
+        const int s = 32 * blk + 4 * step + g;
+        if (s < p.S) {
+          uint32_t w[8];
+          load16(base + (long long)s * ss, w);
+          float f[16];
+          unpack16(w, f);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], fabsf(f[k]));
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
+      mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 16));
+    }
+    if (g == 0) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) red[warp][16 * L + k] = mx[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      float m = red[0][threadIdx.x];
+#pragma unroll
+      for (int w2 = 1; w2 < 8; ++w2) m = fmaxf(m, red[w2][threadIdx.x]);
+      if (m > 0.0f) atomicMax(&p.vmax[(long long)bh * 128 + threadIdx.x], __float_as_uint(m));
+    }
+    return;
+  }
+
+  if (blk >= p.nblk) return;
+  uint32_t x[8][8];
+  load_rows(p, task, bh, blk, lane, x);
+
+  // ---------------------------------------------------------- K smoothing (optional)
+  // the value quantised is fl32(k - mean[channel]); it is formed again, bit for
+  // bit, for the codes below
+  float mu[16];
+  const bool smooth = (task == 1 && p.kmean != nullptr);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mu[i] = smooth ? __ldg(p.kmean + (long long)bh * 128 + 16 * L + i) : 0.0f;
+
   // ---------------------------------------------------------- block maximum and INT8 codes
   float a = 0.0f;
 #pragma unroll
@@ -206,7 +233,7 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
       float f[16];
       unpack16(x[step], f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
+      for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(smooth ? __fsub_rn(f[i], mu[i]) : f[i]));
     }
   }
 #pragma unroll
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
       unpack16(x[step], f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        int v = __float2int_rn(__fmul_rn(f[i], inv));
+        int v = __float2int_rn(__fmul_rn(smooth ? __fsub_rn(f[i], mu[i]) : f[i], inv));
         v = max(-127, min(127, v));
         q[i >> 2] |= (uint32_t)(v & 0xff) << (8 * (i & 3));
       }
@@ -237,6 +264,58 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
     }
     p.scales[task][(long long)bh * p.nblk + blk] = sc;
   }
+}
+
+// ------------------------------------------------------------------ K smoothing
+// mean[b, h, c] = (sum over s < S of K[b, s, h, c]) / S, K after the optional
+// RMSNorm + RoPE, in a fixed binary32 order so that the mean (which decides
+// INT8 codes) is a deterministic function of K.  Per 32-row block j the lanes
+// g = 0..3 of a channel group hold rows 32j + 4t + g (t = 0..7):
+//   P_g = (((0 + x[32j+g]) + x[32j+4+g]) + ...) + x[32j+28+g]
+//   B_j = (P_0 + P_1) + (P_2 + P_3)                      (two xor shuffles)
+// and the blocks are then added in ascending j from 0, and divided by S.
+// Rows >= S load as +0, which leaves every sum unchanged.
+
+// One warp per (b, h, block), as the quantiser: block sums B_j into partial[bh][j][128].
+__global__ void __launch_bounds__(256) prep_kmean_partial_kernel(const QKParams p, float* __restrict__ partial) {
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x * 8 + warp;
+  if (blk >= p.nblk) return;
+  const int g = lane >> 3;
+  const int L = lane & 7;
+  uint32_t x[8][8];
+  load_rows(p, 1, bh, blk, lane, x);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    float f[16];
+    unpack16(x[step], f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 8));    // P_g + P_(g^1)
+    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 16));   // + the other pair
+  }
+  if (g == 0) {
+    float4* dst = reinterpret_cast<float4*>(partial + ((long long)bh * p.nblk + blk) * 128 + 16 * L);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+  }
+}
+
+// One thread per (b, h, channel): the block sums in ascending order, then / S.
+__global__ void __launch_bounds__(128) prep_kmean_kernel(const float* __restrict__ partial, int nblk, int S,
+                                                         float* __restrict__ mean) {
+  const int bh = blockIdx.x, c = threadIdx.x;
+  const float* src = partial + (long long)bh * nblk * 128 + c;
+  float total = 0.0f;
+  for (int j = 0; j < nblk; ++j) total = __fadd_rn(total, __ldg(src + (long long)j * 128));
+  mean[(long long)bh * 128 + c] = __fdiv_rn(total, (float)S);
 }
 
 struct VParams {
@@ -363,6 +442,16 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   p.scales[1] = a.k_scale;
   p.c_log2 = a.c_log2;
   p.vmax = a.vmax;
+  p.kmean = a.k_mean;
+  if (a.k_mean != nullptr) {
+    dim3 g0((nblk + 7) / 8, a.B * a.H, 1);
+    prep_kmean_partial_kernel<<<g0, 256, 0, stream>>>(p, a.k_partial);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prep_kmean_kernel<<<a.B * a.H, 128, 0, stream>>>(a.k_partial, nblk, a.S, a.k_mean);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   dim3 g1((nblk + 7) / 8, a.B * a.H, 3);
   prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
   e = cudaGetLastError();

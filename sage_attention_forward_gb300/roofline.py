@@ -59,3 +59,13 @@ def prepare_bytes(B: int, H: int, S: int, S_pad: int, D: int = 128, rms_norm: bo
     if rope_dim:
         extra += 2 * S * rope_dim * 2     # cos and sin tables, read once
     return read + reread_v + write + scales + extra
+
+
+def prepare_smooth_k_bytes(B: int, H: int, S: int, S_pad: int, D: int = 128, rms_norm: bool = False,
+                           rope_dim: int = 0) -> int:
+    """prepare_bytes plus K smoothing: one more pass over K for its block sums,
+    which are written once and read once, and the per-channel means."""
+    extra_k = B * S * H * D * 2
+    partials = 2 * B * H * (S_pad // 32) * D * 4
+    means = 2 * B * H * D * 4
+    return prepare_bytes(B, H, S, S_pad, D, rms_norm, rope_dim) + extra_k + partials + means

@@ -83,6 +83,27 @@ def test_sage_prepare_rejects_bad_arguments(kw, status):
     assert call_prepare(**kw) == status
 
 
+def call_prepare_smooth(k_mean=FAKE, ws_bytes=None, S_pad=256, rope_dim=0):
+    L = sa.lib()
+    st = I64x3(256 * 2 * 128, 256, 128)
+    if ws_bytes is None:
+        ws_bytes = L.sage_prepare_smooth_k_workspace_size(1, 2, S_pad)
+    return L.sage_prepare_smooth_k(FAKE, FAKE, FAKE, 1, 256, 2, 128, st, st, st, 0.088, None, None, 1e-6, None, None,
+                                   rope_dim, S_pad, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, k_mean, FAKE, ws_bytes, None)
+
+
+def test_sage_prepare_smooth_k_workspace_and_rejections():
+    L = sa.lib()
+    # V maxima (B*H*128 words) + one float per (b, h, 32-row block, channel)
+    assert L.sage_prepare_smooth_k_workspace_size(2, 3, 256) == 2 * 3 * 128 * 4 + 2 * 3 * 8 * 128 * 4
+    assert L.sage_prepare_smooth_k_workspace_size(0, 3, 256) == 0
+    assert call_prepare_smooth(k_mean=None) == 1
+    assert call_prepare_smooth(k_mean=FAKE + 4) == 2
+    assert call_prepare_smooth(ws_bytes=L.sage_prepare_workspace_size(1, 2)) == 1   # the plain size is too small
+    assert call_prepare_smooth(S_pad=200) == 1
+    assert call_prepare_smooth(rope_dim=64) == 1                                       # tables missing
+
+
 def test_sage_attn_fwd_rejects_bad_arguments():
     L = sa.lib()
     st = I64x3(256 * 2 * 128, 256, 128)
