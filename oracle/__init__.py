@@ -29,6 +29,10 @@ Functions and the passages they follow:
                     value of the INT8/e4m3 format the Sage forward consumes
                     (same pull request, commit message of
                     gfx1201_sage_attention), with no further rounding.
+  sage_attention_v16 -- the same with V taken from the BF16 input (the Sage
+                    mode whose P V product is 16-bit: "P and V ... in FP8
+                    or FP16", ai-infra handbook chapter above, section
+                    "SageAttention: quantizing attention too").
   e4m3_encode / e4m3_decode / f32_to_bf16 -- the scalar encoders.
 """
 from __future__ import annotations
@@ -67,6 +71,8 @@ def lib():
         L.oracle_sage_attention.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, c_p,
                                             ctypes.c_int]
+        L.oracle_sage_attention_v16.argtypes = [c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, c_p, ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_init()
         _lib = L
@@ -214,6 +220,26 @@ def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool =
     out = np.empty((len(flat), 128), dtype=np.float64)
     lib().oracle_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs), _ptr(ks), _ptr(vs), B, S, H, int(S_pad),
                                 _ptr(flat), len(flat), int(abs_v), int(p_e4m3), _ptr(out), int(nthreads))
+    return out
+
+
+def sage_attention_v16(prep: dict, v: torch.Tensor, rows: torch.Tensor, abs_v: bool = False,
+                       nthreads: int = 0) -> np.ndarray:
+    """FP64 attention of the prepared INT8 Q/K codes with V taken from the BF16
+    input v [B, S, H, 128] (the Sage mode with a 16-bit P V product), for query
+    rows (b, s, h) -> [n, 128] float64."""
+    q8 = np.ascontiguousarray(prep["q_i8"].numpy())
+    k8 = np.ascontiguousarray(prep["k_i8"].numpy())
+    qs = np.ascontiguousarray(prep["q_scale"].numpy())
+    ks = np.ascontiguousarray(prep["k_scale"].numpy())
+    B, S, H, D = v.shape
+    vb = _bf16_bits(v)
+    S_pad = q8.shape[2]
+    r = rows.to(torch.int64)
+    flat = ((r[:, 0] * S + r[:, 1]) * H + r[:, 2]).contiguous().numpy()
+    out = np.empty((len(flat), 128), dtype=np.float64)
+    lib().oracle_sage_attention_v16(_ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(vb), B, S, H, int(S_pad),
+                                    _ptr(flat), len(flat), int(abs_v), _ptr(out), int(nthreads))
     return out
 
 

@@ -470,6 +470,62 @@ void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8
     }
 }
 
+/*
+ * The same FP64 attention for the Sage mode whose P V product keeps V in 16-bit
+ * precision: Q K^T on the INT8 codes as above, "P and V ... in FP8 or FP16"
+ * (ai-infra handbook, "Kernel acceleration: attention, compilation and
+ * fusion", section "SageAttention: quantizing attention too"), read here as
+ * V taken from the BF16 input itself (no V quantisation):
+ *   O[r, d] = sum_{j < S} 2^(t_j - max t) v[j, d] / sum_{j < S} 2^(t_j - max t),
+ *   v[j, d] = the BF16 V of (b, j, h, d)
+ * with t_j as in oracle_sage_attention and nothing rounded.  v: [B, S, H, 128]
+ * BF16 bits.  abs_v != 0 weights |v| instead.
+ */
+void oracle_sage_attention_v16(const int8_t* q8, const int8_t* k8, const float* qs, const float* ks,
+                               const uint16_t* v, int B, int S, int H, int64_t S_pad, const int64_t* rows,
+                               int64_t n_rows, int abs_v, double* out, int nthreads) {
+    int64_t nblk = S_pad / 32;
+    (void)B;
+    (void)nthreads;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        double* t = (double*)malloc(sizeof(double) * (size_t)S);
+        double acc[128];
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; i++) {
+            int64_t r = rows[i];
+            int64_t h = r % H, s = (r / H) % S, b = r / ((int64_t)H * S);
+            int64_t bh = b * H + h;
+            const int8_t* qrow = q8 + (bh * S_pad + s) * 128;
+            double fq = (double)qs[bh * nblk + s / 32];
+            double tmax = -INFINITY;
+            for (int64_t j = 0; j < S; j++) {
+                const int8_t* krow = k8 + (bh * S_pad + j) * 128;
+                int64_t dot = 0;
+                for (int d = 0; d < 128; d++) dot += (int64_t)qrow[d] * (int64_t)krow[d];
+                t[j] = (double)dot * fq * (double)ks[bh * nblk + j / 32];
+                if (t[j] > tmax) tmax = t[j];
+            }
+            double wsum = 0.0;
+            for (int d = 0; d < 128; d++) acc[d] = 0.0;
+            for (int64_t j = 0; j < S; j++) {
+                double w = exp2(t[j] - tmax);
+                wsum += w;
+                const uint16_t* vrow = v + ((b * S + j) * H + h) * 128;
+                for (int d = 0; d < 128; d++) {
+                    double vv = (double)oracle_bf16_to_f32(vrow[d]);
+                    acc[d] += w * (abs_v ? fabs(vv) : vv);
+                }
+            }
+            for (int d = 0; d < 128; d++) out[i * 128 + d] = acc[d] / wsum;
+        }
+        free(t);
+    }
+}
+
 void oracle_init(void) { e4m3_init(); }
 
 int oracle_num_threads(void) {
