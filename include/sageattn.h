@@ -232,6 +232,31 @@ ATTN_API attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const
                           attn_stream_t stream);
 
 /*
+ * sage_attn_fwd_pv16 -- the Sage forward with a 16-bit P V product: Q K^T on
+ * the INT8 codes exactly as sage_attn_fwd, then P (BF16) times V taken from the
+ * BF16 input itself, FP32 accumulation, BF16 output.  The handbook's
+ * SageAttention section has P and V "in FP8 or FP16" (ai-infra handbook,
+ * "Kernel acceleration: attention, compilation and fusion", section
+ * "SageAttention: quantizing attention too"); this is the 16-bit choice,
+ * with BF16 because V arrives in BF16.  It trades the FP8 product's speed for
+ * accuracy: V is not quantised and P carries 8 significant bits instead of 4.
+ *   O[r, d] = sum_j p[r, j] v[j, d] / sum_j p[r, j],  p = bf16(2^(t - m_r)),
+ *   t as in sage_attn_fwd, m_r the row's reference maximum (moved only when a
+ *   tile's maximum passes it by more than 8 log2 units), the denominator summed
+ *   from the unrounded p in FP32.
+ *   q_i8, k_i8, q_scale, k_scale : from sage_prepare or sage_prepare_smooth_k
+ *                (its v_fp8 / v_scale outputs are not read)
+ *   v          : const BF16 [B, S, H, 128] with element strides v_str
+ *   o, o_str, B, S, H, D, S_pad, workspace, workspace_bytes : as sage_attn_fwd
+ * Enqueues two kernels on `stream`.  Errors as sage_attn_fwd, plus v's
+ * checks (NULL, alignment, strides) as attn_fwd_bf16.
+ */
+ATTN_API attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale,
+                                        const float* k_scale, const void* v, const int64_t v_str[3], void* o,
+                                        const int64_t o_str[3], int B, int S, int H, int D, int64_t S_pad,
+                                        void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_get_device_status -- synchronise `stream`, then read and clear the
  * device error words of all kernels.  ATTN_OK if no bounded wait ran out
  * since the last call, ATTN_ERR_DEVICE_TIMEOUT otherwise, ATTN_ERR_CUDA if

@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
         L.sage_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _I64x3, i, i, i, i, ctypes.c_int64, _vp,
                                     ctypes.c_size_t, _vp]
         L.sage_attn_fwd.restype = i
+        L.sage_attn_fwd_pv16.argtypes = [_vp, _vp, _vp, _vp, _vp, _I64x3, _vp, _I64x3, i, i, i, i, ctypes.c_int64,
+                                         _vp, ctypes.c_size_t, _vp]
+        L.sage_attn_fwd_pv16.restype = i
         L.attn_get_device_status.argtypes = [_vp]
         L.attn_get_device_status.restype = i
         L.attn_last_error.argtypes = []
@@ -252,11 +255,35 @@ def sage_attn_fwd(prep: Prepared, out: torch.Tensor | None = None, workspace: to
     return out
 
 
+def sage_attn_fwd_pv16(prep: Prepared, v: torch.Tensor, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Attention on prepared INT8 Q/K with a 16-bit P V product: P in BF16 times
+    the BF16 input v [B, S, H, 128] (not quantised) -> BF16 [B, S, H, 128]."""
+    B, H, S_pad, D = prep.q_i8.shape
+    S = prep.S
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=prep.q_i8.device)
+    if workspace is None:
+        workspace = attn_workspace(B, H, S_pad, prep.q_i8.device)
+    vs, os_ = _bshd("v", v), _bshd("out", out)
+    _check(lib().sage_attn_fwd_pv16(prep.q_i8.data_ptr(), prep.k_i8.data_ptr(), prep.q_scale.data_ptr(),
+                                    prep.k_scale.data_ptr(), v.data_ptr(), vs, out.data_ptr(), os_, B, S, H, D,
+                                    int(S_pad), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+    return out
+
+
 def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
-                   rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False) -> torch.Tensor:
-    """Prepare + attention: the SageAttention-style forward of BF16 Q/K/V."""
+                   rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3") -> torch.Tensor:
+    """Prepare + attention: the SageAttention-style forward of BF16 Q/K/V.
+
+    pv="e4m3": P and V in FP8 (sage_attn_fwd); pv="bf16": P in BF16 times the
+    unquantised V (sage_attn_fwd_pv16)."""
+    if pv not in ("e4m3", "bf16"):
+        raise ValueError(f"pv must be 'e4m3' or 'bf16', not {pv!r}")
     prep = sage_prepare(q, k, v, softmax_scale, None, q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim,
                         stream=stream, smooth_k=smooth_k)
+    if pv == "bf16":
+        return sage_attn_fwd_pv16(prep, v, out=out, stream=stream)
     return sage_attn_fwd(prep, out=out, stream=stream)
 
 

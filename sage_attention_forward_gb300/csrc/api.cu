@@ -429,6 +429,46 @@ attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t*
   return ATTN_OK;
 }
 
+attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale, const float* k_scale,
+                               const void* v, const int64_t v_str[3], void* o, const int64_t o_str[3], int B, int S,
+                               int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                               attn_stream_t stream) {
+  TRY(check_shape(B, S, H, D));
+  if (S_pad < S || S_pad % 128 != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
+  if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  struct {
+    const char* n;
+    const void* p;
+  } ins[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"q_scale", q_scale}, {"k_scale", k_scale}, {"workspace", workspace}};
+  for (auto& t : ins) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  if (workspace_bytes < sage_attn_workspace_size(B, H, S_pad))
+    return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
+                sage_attn_workspace_size(B, H, S_pad));
+  long long vs[3], os[3];
+  TRY(check_strides("v", v, v_str, B, S, H, vs));
+  TRY(check_strides("o", o, o_str, B, S, H, os));
+  TRY(check_device());
+  TRY(get_encoder());
+  const long long bh = (long long)B * H;
+  const long long n_codes = bh * S_pad * 128;
+  uint8_t* q16 = reinterpret_cast<uint8_t*>(workspace);
+  uint8_t* k16 = q16 + 2 * n_codes;
+  CUtensorMap tq, tk, tv;
+  TRY(tmap_f16_rows(&tq, q16, S_pad, bh));
+  TRY(tmap_f16_rows(&tk, k16, S_pad, bh));
+  TRY(tmap_bhsd_bf16(&tv, v, B, S, H, vs));
+  cudaError_t e = sa::launch_sage_widen(q_i8, k_i8, q16, k16, n_codes, sa::device_sm_count(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd_pv16 widen launch");
+  e = sa::launch_sage_attn_pv16(tq, tk, tv, q_scale, k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd_pv16 launch");
+  return ATTN_OK;
+}
+
 attn_status attn_get_device_status(attn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");

@@ -56,6 +56,11 @@ cudaError_t launch_sage_attn(const CUtensorMap& tm_q16, const CUtensorMap& tm_k1
                              const float* q_scale, const float* k_scale, const float* v_scale, void* o,
                              long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
                              cudaStream_t stream);
+// The 16-bit P V mode: V is the BF16 input through a [B, S, H, 128] tensor map.
+cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16,
+                                  const CUtensorMap& tm_v_bf16, const float* q_scale, const float* k_scale, void* o,
+                                  long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                  long long S_pad, cudaStream_t stream);
 cudaError_t read_and_clear_err_sage(uint32_t* out);
 
 }  // namespace sa

@@ -48,21 +48,40 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kNQ = 2;
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
 constexpr int kQTileBytes = 128 * 128 * 2;   // FP16 128 x 128
 constexpr int kHalfBytes = kQTileBytes / 2;  // [128 rows][64 columns] FP16 sub-tile
-constexpr int kVTileBytes = 128 * 128;       // e4m3 [128 d][128 positions]
 constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
-constexpr float kTau = 4.0f;
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
+// The P V product: FP8 (P e4m3 x V e4m3 from the prepare) or 16-bit (P BF16 x
+// the BF16 V input, no V quantisation; the higher-accuracy mode).
+enum class PV { kE4M3, kBF16 };
+template <PV kPV>
+struct Cfg;
+template <>
+struct Cfg<PV::kE4M3> {
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 3;
+  static constexpr int kVTileBytes = 128 * 128;       // e4m3 [128 d][128 positions]
+  static constexpr float kTau = 4.0f;
+};
+template <>
+struct Cfg<PV::kBF16> {
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = 2;
+  static constexpr int kVTileBytes = 128 * 128 * 2;   // BF16 [128 keys][128 d] as two 64-channel halves
+  static constexpr float kTau = 8.0f;
+};
+
+template <PV kPV>
 struct __align__(1024) Smem {
+  static constexpr int kKStages = Cfg<kPV>::kKStages;
+  static constexpr int kVStages = Cfg<kPV>::kVStages;
   uint8_t q[kNQ][kQTileBytes];
   uint8_t k[kKStages][kQTileBytes];
-  uint8_t v[kVStages][kVTileBytes];
+  uint8_t v[kVStages][Cfg<kPV>::kVTileBytes];
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -79,7 +98,7 @@ __device__ uint32_t g_err_sage;
 struct Params {
   const float* q_scale;   // [B*H, nblk]
   const float* k_scale;   // [B*H, nblk]
-  const float* v_scale;   // [B*H, 128]
+  const float* v_scale;   // [B*H, 128] (FP8 mode)
   __nv_bfloat16* o;
   long long o_sb, o_ss, o_sh;
   int S;
@@ -91,11 +110,17 @@ struct Params {
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
+template <PV kPV>
 __global__ void __launch_bounds__(kThreads, 1)
     sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  constexpr int kKStages = Cfg<kPV>::kKStages;
+  constexpr int kVStages = Cfg<kPV>::kVStages;
+  constexpr int kVTileBytes = Cfg<kPV>::kVTileBytes;
+  constexpr float kTau = Cfg<kPV>::kTau;
+  constexpr bool kFP8 = (kPV == PV::kE4M3);
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<kPV>& sm = *reinterpret_cast<Smem<kPV>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -163,7 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&sm.v_full[slot], kVTileBytes);
-          tma_load_3d(sm.v[slot], &tm_v, &sm.v_full[slot], j * kBN, 0, bh);
+          if constexpr (kFP8) {
+            tma_load_3d(sm.v[slot], &tm_v, &sm.v_full[slot], j * kBN, 0, bh);
+          } else {
+            // V_j from the BF16 input [B, S, H, 128]: keys j*128.. (rows past S read as 0), two channel halves
+            tma_load_4d(sm.v[slot], &tm_v, &sm.v_full[slot], 0, j * kBN, bh % p.H, bh / p.H);
+            tma_load_4d(sm.v[slot] + kHalfBytes, &tm_v, &sm.v_full[slot], 64, j * kBN, bh % p.H, bh / p.H);
+          }
           v_issued = j + 1;
         }
       }
@@ -183,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool leader = elect_one();
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_qk = idesc_f32acc(kFmtF16, kFmtF16, false, false, kBM, kBN);
-      const uint32_t idesc_pv = idesc_f32acc(kFmtE4M3, kFmtE4M3, false, false, kBM, 128);
+      const uint32_t idesc_pv = kFP8 ? idesc_f32acc(kFmtE4M3, kFmtE4M3, false, false, kBM, 128)
+                                     : idesc_f32acc(kFmtBF16, kFmtBF16, false, true, kBM, 128);
       // TMEM columns of S_i and O_i
       auto tS = [&](int i) { return tmem + 128u * (uint32_t)i; };
       auto tO = [&](int i) { return tmem + 256u + 128u * (uint32_t)i; };
@@ -198,15 +230,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) mma_f16_ss(tS(i), da, db, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      // O_i += P_i V for keys [64*half, 64*half + 64): 2 steps of 32 positions (bytes)
-      // inside the 128-byte swizzled rows of V^T
+      // O_i += P_i V for keys [64*half, 64*half + 64).  FP8: 2 steps of 32 positions
+      // (bytes) inside the 128-byte swizzled rows of V^T.  BF16: 4 steps of 16 keys
+      // (rows of 128 bytes) of the MN-major V tile, whose two 64-channel halves are
+      // 16 KB apart.  Either way a step's P is 8 TMEM columns.
       auto issue_pv_half = [&](int i, int slot, int half, bool acc) {
         const uint32_t va = smem_u32(sm.v[slot]);
+        if constexpr (kFP8) {
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int kk = 2 * half + k2;
-          const uint64_t db = smem_desc_sw128(va + kk * 32, 16, 1024);
-          if (leader) mma_f8_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int kk = 2 * half + k2;
+            const uint64_t db = smem_desc_sw128(va + kk * 32, 16, 1024);
+            if (leader) mma_f8_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * half + k4;
+            const uint64_t db = smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024);
+            if (leader) mma_f16_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          }
         }
       };
       auto issue_pv = [&](int i, int slot, int j) -> bool {
@@ -319,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= sc;
         m_used = m_cand;
       }
-      const float off = m_used + kTau - kLog2_448;
+      // FP8: p' = 448 2^-kTau 2^(t - m) fills the e4m3 range; BF16: p = 2^(t - m) <= 2^kTau
+      const float off = kFP8 ? m_used + kTau - kLog2_448 : m_used;
       float rs0 = 0.0f, rs1 = 0.0f;
       // the key mask only exists in the tile that holds the ragged tail, so the loop is
       // compiled twice rather than carrying 128 predicated selects through every tile
@@ -327,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-          // 32 scores of key block blk -> 8 words of four e4m3 each, P columns [8blk, 8blk + 8)
-          uint32_t pk[8];
+          // 32 scores of key block blk -> 8 words of four e4m3 each (FP8) or 16 words of
+          // two BF16 each (BF16)
+          uint32_t pk[kFP8 ? 8 : 16];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             float x0, x1, x2, x3;
@@ -348,9 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fadd2(rs0, rs1, rs0, rs1, p0, p1);
             fadd2(rs0, rs1, rs0, rs1, p2, p3);
-            pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+            if constexpr (kFP8) {
+              pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+            } else {
+              pk[2 * e] = pack_bf16x2(p0, p1);
+              pk[2 * e + 1] = pack_bf16x2(p2, p3);
+            }
           }
-          tmem_st8(tS + 8 * blk, pk);
+          // P columns: FP8 [8blk, 8blk + 8) (four per column), BF16 [16blk, 16blk + 16) (two per column)
+          if constexpr (kFP8) {
+            tmem_st8(tS + 8 * blk, pk);
+          } else {
+            tmem_st16(tS + 16 * blk, pk);
+          }
           if (blk & 1) {
             if (blk == 1 && j > 0 && __any_sync(0xffffffffu, need)) {
               // O_i must hold P_{j-1} V_{j-1} before it is rescaled, and be rescaled
@@ -388,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n > 0 && mbar_wait_warp<true>(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float* vs = p.v_scale + (long long)bh * 128;
+      const float* vs = kFP8 ? p.v_scale + (long long)bh * 128 : nullptr;
       const int b = bh / p.H, h = bh % p.H;
       __nv_bfloat16* dst = p.o + (long long)b * p.o_sb + (long long)grow * p.o_ss + (long long)h * p.o_sh;
 #pragma unroll
@@ -399,8 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 sv = __ldg(reinterpret_cast<const float2*>(vs + 32 * cc + 2 * e));
-          w[e] = pack_bf16x2(u2f(o[2 * e]) * (sv.x * inv_l), u2f(o[2 * e + 1]) * (sv.y * inv_l));
+          if constexpr (kFP8) {
+            const float2 sv = __ldg(reinterpret_cast<const float2*>(vs + 32 * cc + 2 * e));
+            w[e] = pack_bf16x2(u2f(o[2 * e]) * (sv.x * inv_l), u2f(o[2 * e + 1]) * (sv.y * inv_l));
+          } else {
+            w[e] = pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l);
+          }
         }
         if (grow < p.S) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
@@ -448,9 +507,45 @@ __global__ void __launch_bounds__(256) widen_i8_f16_kernel(const int8_t* __restr
   }
 }
 
+template <PV kPV>
+size_t smem_bytes_of() {
+  return sizeof(Smem<kPV>) + 1024;
+}
+
+template <PV kPV>
+cudaError_t launch_kernel(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, const CUtensorMap& tm_v,
+                          const float* q_scale, const float* k_scale, const float* v_scale, void* o, long long o_sb,
+                          long long o_ss, long long o_sh, int B, int S, int H, long long S_pad, cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  const size_t smem = smem_bytes_of<kPV>();
+  if (!attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(sage_attn_kernel<kPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  Params p;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.o_sb = o_sb;
+  p.o_ss = o_ss;
+  p.o_sh = o_sh;
+  p.S = S;
+  p.H = H;
+  p.nblk = (int)(S_pad / 32);
+  p.n_tiles = (S + kBN - 1) / kBN;
+  dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
+  sage_attn_kernel<kPV><<<grid, kThreads, smem, stream>>>(tm_q16, tm_k16, tm_v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-size_t sage_attn_smem_bytes() { return sizeof(Smem) + 1024; }
+size_t sage_attn_smem_bytes() { return smem_bytes_of<PV::kE4M3>(); }
 
 cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,
                               int num_sms, cudaStream_t stream) {
@@ -469,30 +564,16 @@ cudaError_t launch_sage_attn(const CUtensorMap& tm_q16, const CUtensorMap& tm_k1
                              const float* q_scale, const float* k_scale, const float* v_scale, void* o,
                              long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
                              cudaStream_t stream) {
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  const size_t smem = sage_attn_smem_bytes();
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(sage_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  Params p;
-  p.q_scale = q_scale;
-  p.k_scale = k_scale;
-  p.v_scale = v_scale;
-  p.o = reinterpret_cast<__nv_bfloat16*>(o);
-  p.o_sb = o_sb;
-  p.o_ss = o_ss;
-  p.o_sh = o_sh;
-  p.S = S;
-  p.H = H;
-  p.nblk = (int)(S_pad / 32);
-  p.n_tiles = (S + kBN - 1) / kBN;
-  dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
-  sage_attn_kernel<<<grid, kThreads, smem, stream>>>(tm_q16, tm_k16, tm_v8, p);
-  return cudaGetLastError();
+  return launch_kernel<PV::kE4M3>(tm_q16, tm_k16, tm_v8, q_scale, k_scale, v_scale, o, o_sb, o_ss, o_sh, B, S, H,
+                                  S_pad, stream);
+}
+
+cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16,
+                                  const CUtensorMap& tm_v_bf16, const float* q_scale, const float* k_scale, void* o,
+                                  long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                  long long S_pad, cudaStream_t stream) {
+  return launch_kernel<PV::kBF16>(tm_q16, tm_k16, tm_v_bf16, q_scale, k_scale, nullptr, o, o_sb, o_ss, o_sh, B, S,
+                                  H, S_pad, stream);
 }
 
 cudaError_t read_and_clear_err_sage(uint32_t* out) {

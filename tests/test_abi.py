@@ -115,6 +115,23 @@ def test_sage_attn_fwd_rejects_bad_arguments():
     assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 96, 256, FAKE, ok_ws, None) == 3
 
 
+def test_sage_attn_fwd_pv16_rejects_bad_arguments():
+    L = sa.lib()
+    st = I64x3(256 * 2 * 128, 256, 128)
+    ws = L.sage_attn_workspace_size(1, 2, 256)
+
+    def call(q8=FAKE, v=FAKE, vst=st, S_pad=256, D=128, ws_bytes=ws):
+        return L.sage_attn_fwd_pv16(q8, FAKE, FAKE, FAKE, v, vst, FAKE, st, 1, 256, 2, D, S_pad, FAKE, ws_bytes, None)
+
+    assert call(q8=None) == 1
+    assert call(v=None) == 1
+    assert call(v=FAKE + 2) == 2
+    assert call(vst=I64x3(256 * 2 * 128, 250, 128)) == 2      # s-stride not a multiple of 8 elements
+    assert call(S_pad=200) == 1
+    assert call(ws_bytes=ws - 1) == 1
+    assert call(D=64) == 3
+
+
 def test_product_path_does_not_import_the_oracle():
     import subprocess
     import sys
