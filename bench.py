@@ -37,16 +37,19 @@ METRIC = "attention TFLOPS (4·B·H·S²·D/s) at S=76112,H=40,D=128; % of tenso
 KERNELS_PER_STEP = 5  # attn_bf16, prep_qk_vmax, prep_v, widen_i8_f16, sage_attn
 
 
-def kernel_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken (or no summary)."""
+def kernel_traffic(record: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary profiles/<record>_traffic.json,
+    or None when a source file the record lists changed since the counters were taken
+    (or there is no record)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"{record}_traffic.json")
     if workload != "wan720p" or not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    srcs = ["sage_attention_forward_gb300/csrc/ptx.cuh", f"sage_attention_forward_gb300/csrc/{kernel}.cu"]
+    srcs = rec.get("sources", [])
+    if not srcs or not all(os.path.exists(os.path.join(ROOT, p)) for p in srcs):
+        return None
     h = hashlib.sha256(b"".join(open(os.path.join(ROOT, p), "rb").read() for p in srcs)).hexdigest()
     if h != rec.get("kernel_source_sha256"):
         return None
@@ -184,44 +187,73 @@ def run_ours(args, rank, world):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
+    # the step's own split (each call timed inside the interleaved step)
     per = {"bf16": [], "prepare": [], "sage_core": []}
     for e in evs:
         per["bf16"].append(e[0].elapsed_time(e[1]))
         per["prepare"].append(e[1].elapsed_time(e[2]))
         per["sage_core"].append(e[2].elapsed_time(e[3]))
     F = roofline.attention_flops(B, H, S, D)
-    ms = {k2: statistics.mean(v2) for k2, v2 in per.items()}
-    ms["sage"] = ms["prepare"] + ms["sage_core"]
-    prep_bytes = roofline.prepare_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
+    step_ms = {k2: statistics.mean(v2) for k2, v2 in per.items()}
     peaks = load_peaks()
-    bf16_tflops = F / (ms["bf16"] * 1e-3) / 1e12
-    providers = {
-        "bf16": {"ms": ms["bf16"], "tflops": bf16_tflops},
-        "sage": {"ms": ms["sage"], "tflops": F / (ms["sage"] * 1e-3) / 1e12},
-        "sage_core": {"ms": ms["sage_core"], "tflops": F / (ms["sage_core"] * 1e-3) / 1e12,
-                      # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
-                      "frac_of_tensor_roof": (F / (ms["sage_core"] * 1e-3) / 1e12) /
-                      (peaks["bf16_sustained"] / 0.75)},
-        "prepare": {"ms": ms["prepare"], "gbs": prep_bytes / (ms["prepare"] * 1e-3) / 1e9,
-                    "frac_of_hbm": prep_bytes / (ms["prepare"] * 1e-3) / 1e9 / peaks["hbm"]},
-    }
 
-    # the K-smoothing prepare (not part of the step): timed alone, after the step's timed region
+    # providers, each timed on its own: 2 warm-up + 5 back-to-back calls, 3 rounds with the
+    # providers interleaved, median.  Inside the step the GPU's power management carries
+    # clock headroom from one kernel into the next, which skews a per-call split.
+    o_pv16 = torch.empty_like(o_bf16)
     prep_s = sa.Prepared.empty(B, H, S, S_pad, dev)
     ws_s = sa.prepare_workspace(B, H, dev, S_pad, smooth_k=True)
-    for _ in range(2):
-        sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep_s, workspace=ws_s, smooth_k=True, **kw)
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    ev_s[0].record(stream)
-    for _ in range(5):
-        sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep_s, workspace=ws_s, smooth_k=True, **kw)
-    ev_s[1].record(stream)
+    calls = {
+        "bf16": lambda: sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale),
+        "sage": lambda: (sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw),
+                         sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)),
+        "sage_core": lambda: sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a),
+        "sage_pv16_core": lambda: sa.sage_attn_fwd_pv16(prep, v, out=o_pv16, workspace=ws_a),
+        "prepare": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p,
+                                           **kw),
+        "prepare_smooth_k": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep_s,
+                                                    workspace=ws_s, smooth_k=True, **kw),
+    }
+    rounds = {name: [] for name in calls}
+    for _ in range(3):
+        for name, fn in calls.items():
+            for _ in range(2):
+                fn()
+            ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev_p[0].record(stream)
+            for _ in range(5):
+                fn()
+            ev_p[1].record(stream)
+            ev_p[1].synchronize()
+            rounds[name].append(ev_p[0].elapsed_time(ev_p[1]) / 5)
     sa.attn_get_device_status()
-    ms_s = ev_s[0].elapsed_time(ev_s[1]) / 5
+    ms = {name: statistics.median(t) for name, t in rounds.items()}
+    prep_bytes = roofline.prepare_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
     smooth_bytes = roofline.prepare_smooth_k_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
-    providers["prepare_smooth_k"] = {"ms": ms_s, "gbs": smooth_bytes / (ms_s * 1e-3) / 1e9,
-                                     "frac_of_hbm": smooth_bytes / (ms_s * 1e-3) / 1e9 / peaks["hbm"]}
-    del prep_s, ws_s
+
+    def tf(name):
+        return F / (ms[name] * 1e-3) / 1e12
+
+    bf16_tflops = tf("bf16")
+    # the roofline's kernel time is its average launch inside the timed region
+    roof_tflops = F / (step_ms["bf16"] * 1e-3) / 1e12
+    providers = {
+        "bf16": {"ms": ms["bf16"], "tflops": bf16_tflops},
+        "sage": {"ms": ms["sage"], "tflops": tf("sage")},
+        "sage_core": {"ms": ms["sage_core"], "tflops": tf("sage_core"),
+                      # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
+                      "frac_of_tensor_roof": tf("sage_core") / (peaks["bf16_sustained"] / 0.75)},
+        "sage_pv16_core": {"ms": ms["sage_pv16_core"], "tflops": tf("sage_pv16_core"),
+                           "frac_of_tensor_roof": tf("sage_pv16_core") / peaks["bf16_sustained"]},
+        "prepare": {"ms": ms["prepare"], "gbs": prep_bytes / (ms["prepare"] * 1e-3) / 1e9,
+                    "frac_of_hbm": prep_bytes / (ms["prepare"] * 1e-3) / 1e9 / peaks["hbm"]},
+        "prepare_smooth_k": {"ms": ms["prepare_smooth_k"],
+                             "gbs": smooth_bytes / (ms["prepare_smooth_k"] * 1e-3) / 1e9,
+                             "frac_of_hbm": smooth_bytes / (ms["prepare_smooth_k"] * 1e-3) / 1e9 / peaks["hbm"]},
+        "timing": "each provider alone: 2 warm-up + 5 calls, 3 interleaved rounds, median",
+        "in_step_ms": step_ms,
+    }
+    del prep_s, ws_s, o_pv16
 
     # ------------------------------------------------------------- end to end
     e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)
@@ -245,10 +277,10 @@ def run_ours(args, rank, world):
                    "step": "attn_fwd_bf16 + sage_prepare + sage_attn_fwd (two attention evaluations)",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "providers": providers,
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": bf16_tflops,
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": roof_tflops,
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": bf16_tflops / peaks["bf16_sustained"],
-                     "traffic": kernel_traffic("attn_bf16", wl.name),
+                     "frac": roof_tflops / peaks["bf16_sustained"],
+                     "traffic": kernel_traffic("attn_fwd_bf16", wl.name),
                      "peak_source": f"{peaks['source']} bf16 sustained"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": e2e,

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsageattn.so")
-SOURCES = ["api.cu", "attn_bf16.cu", "sage_prepare.cu", "sage_attn.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "sage_prepare.cu"]
 HEADERS = ["ptx.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -194,7 +194,7 @@ attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, 
   TRY(tmap_bhsd_bf16(&tk, k, B, S, H, ks));
   TRY(tmap_bhsd_bf16(&tv, v, B, S, H, vs));
   const float c = (float)((double)softmax_scale * kLog2e);
-  cudaError_t e = sa::launch_attn_bf16(tq, tk, tv, o, os[0], os[1], os[2], B, S, H, c, (cudaStream_t)stream);
+  cudaError_t e = sa::launch_attn_fwd_bf16(tq, tk, tv, o, os[0], os[1], os[2], B, S, H, c, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "attn_fwd_bf16 launch");
   return ATTN_OK;
 }
@@ -472,14 +472,12 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
 attn_status attn_get_device_status(attn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-  uint32_t w1 = 0, w2 = 0;
-  e = sa::read_and_clear_err_bf16(&w1);
+  uint32_t w = 0;
+  e = sa::read_and_clear_err_attn(&w);
   if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
-  e = sa::read_and_clear_err_sage(&w2);
-  if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
-  if (w1 | w2)
-    return fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (attn_fwd_bf16 bits 0x%x, sage_attn_fwd bits 0x%x)",
-                w1, w2);
+  if (w)
+    return fail(ATTN_ERR_DEVICE_TIMEOUT,
+                "an attention kernel gave up on a bounded wait (bits 0x%x: 1 TMA load, 2 MMA commit, 4 hand-off)", w);
   return ATTN_OK;
 }
 

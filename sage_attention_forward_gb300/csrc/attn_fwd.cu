@@ -1,39 +1,52 @@
-// SageAttention-style forward on prepared tensors, for sm_103a.
+// The attention forward kernels, for sm_103a: one tcgen05 flash-attention
+// kernel, instantiated for three modes.
 //
-// What it computes (aiter pull request "gfx1201_sage_prepare /
-// gfx1201_sage_attention", commit message of gfx1201_sage_attention;
-// Technical Details): Q K^T on the INT8 codes, online softmax in base 2 (Q's
-// scale already carries softmax_scale * log2(e)), P V with P and V in FP8
-// e4m3, FP32 accumulation, BF16 output:
-//   t[r, j] = (q_i8[r] . k_i8[j]) * q_scale[r / 32] * k_scale[j / 32]
-//   O[r, d] = v_scale[d] * sum_j e4m3(p'[r, j]) v_fp8[d, j] / sum_j p'[r, j]
-//   p'[r, j] = 448 * 2^-kTau * 2^(t[r, j] - m_r)
-// where m_r is the row's reference maximum (see below); the constant factor
-// 448 * 2^-kTau keeps p' inside the e4m3 range and cancels in the ratio.
+//   Mode::kBF16     BF16 Q, K, V (the inputs, [B, S, H, 128] with strides):
+//                   S = Q K^T on BF16, online softmax in base 2 with
+//                   c = softmax_scale * log2(e), P in BF16, O = P V / l in
+//                   FP32, BF16 output.  The flash forward of the ai-infra
+//                   handbook, "Kernel acceleration: attention, compilation and
+//                   fusion", section "Attention: from O(N^2) memory to blocks".
+//   Mode::kSageFP8  the SageAttention-style forward on prepared tensors
+//                   (aiter pull request "gfx1201_sage_prepare /
+//                   gfx1201_sage_attention", commit message of
+//                   gfx1201_sage_attention; Technical Details):
+//                     t[r, j] = (q_i8[r] . k_i8[j]) * q_scale[r / 32] * k_scale[j / 32]
+//                     O[r, d] = v_scale[d] * sum_j e4m3(p'[r, j]) v_fp8[d, j] / sum_j p'[r, j]
+//                     p'[r, j] = 448 * 2^-kTau * 2^(t[r, j] - m_r)
+//                   (Q's scale already carries softmax_scale * log2(e); the
+//                   constant 448 * 2^-kTau keeps p' inside the e4m3 range and
+//                   cancels in the ratio).
+//   Mode::kSagePV16 the same scores, then P in BF16 times the BF16 V input
+//                   (no V quantisation): the 16-bit choice of the handbook's
+//                   "P and V in FP8 or FP16" (section "SageAttention:
+//                   quantizing attention too").
+// m_r is the row's reference maximum: it moves only when a tile's maximum
+// exceeds it by more than kTau (log2 units), and O and l are then rescaled.
 //
 // sm_103a has no INT8 tensor-core MMA (tcgen05 kind::i8 is not accepted for
-// this target), so the codes are widened to FP16 -- exactly, |code| <= 127 --
-// by a streaming pass into the caller's workspace, and Q K^T runs on
-// tcgen05 kind::f16 with an FP32 accumulator.  That product is exact: every
-// partial sum is an integer of magnitude <= 128 * 127^2 < 2^24.  P V runs on
-// tcgen05 kind::f8f6f4 with P (e4m3, four per TMEM column) taken from TMEM
-// and V^T from shared memory, where the [B, H, 128, S_pad] layout makes it the
-// K-major operand directly.
+// this target), so for the Sage modes the codes are widened to FP16 --
+// exactly, |code| <= 127 -- by a streaming pass into the caller's workspace,
+// and Q K^T runs on tcgen05 kind::f16 with an FP32 accumulator.  That product
+// is exact: every partial sum is an integer of magnitude <= 128 * 127^2 < 2^24.
+// The FP8 P V runs on tcgen05 kind::f8f6f4 with P (e4m3, four per TMEM column)
+// from TMEM and V^T from shared memory, where the [B, H, 128, S_pad] layout
+// makes it the K-major operand directly; the 16-bit P V on kind::f16 with P
+// (BF16, two per column) from TMEM and the V tile as the MN-major operand.
 //
-// Structure is that of the BF16 kernel: one CTA = (batch, head, two 128-row
-// Q tiles), 320 threads; warp 8 TMA producer (Q once, then K_j into a 3-slot
-// ring of FP16 tiles and V_j into a 3-slot ring of e4m3 tiles), warp 9 MMA
-// issuer, warps 0-3 and 4-7 one softmax thread per row for Q tile 0 and 1.
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P_i
-// (e4m3) overwrites the first 32 columns of S_i.  The reference maximum moves
-// only when a tile's maximum exceeds it by more than kTau (log2 units).
-// Unlike the BF16 kernel, the two softmax warpgroups are not made to take
-// turns: with the cheaper e4m3 P V product the softmax warps are the busiest
-// units, and overlapping the two warpgroups' sections keeps the SM
-// sub-partitions' issue slots fuller.  The waits on the critical hand-offs
-// (the MMA warp's, and a softmax warpgroup's wait for its S tile) poll; the
-// producer's and the O-rescale waits sleep on their barriers, which gives
-// their issue slots to the softmax warps.
+// One CTA = (batch, head, two 128-row Q tiles), 320 threads: warp 8 TMA
+// producer (Q once, then K_j and V_j into rings of tiles), warp 9 MMA issuer,
+// warps 0-3 and 4-7 one softmax thread per row for Q tile 0 and 1.  TMEM
+// columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P_i
+// overwrites the first 32 (e4m3) or 64 (BF16) columns of S_i.  Per step the MMA
+// warp issues P_0 V_j, S_0 = Q_0 K_{j+1}^T, P_1 V_j, S_1 = Q_1 K_{j+1}^T; each
+// warpgroup publishes its P in two halves of 64 keys, so the P V product of
+// the first half overlaps the exponentials of the second.  The two softmax
+// warpgroups run unsynchronised, so one's section overlaps the other's wait
+// for its S tile.  The waits on the critical hand-offs (the MMA warp's, and a
+// softmax warpgroup's wait for its S tile) poll; the producer's and the
+// O-rescale waits sleep on their barriers, which gives their issue slots to
+// the softmax warps.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -55,33 +68,35 @@ constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
-// The P V product: FP8 (P e4m3 x V e4m3 from the prepare) or 16-bit (P BF16 x
-// the BF16 V input, no V quantisation; the higher-accuracy mode).
-enum class PV { kE4M3, kBF16 };
-template <PV kPV>
+enum class Mode { kBF16, kSageFP8, kSagePV16 };
+template <Mode kMode>
 struct Cfg;
 template <>
-struct Cfg<PV::kE4M3> {
+struct Cfg<Mode::kSageFP8> {
   static constexpr int kKStages = 3;
   static constexpr int kVStages = 3;
   static constexpr int kVTileBytes = 128 * 128;       // e4m3 [128 d][128 positions]
   static constexpr float kTau = 4.0f;
 };
-template <>
-struct Cfg<PV::kBF16> {
+// the two modes with a BF16 V tile ([128 keys][128 d] as two 64-channel halves)
+struct CfgBF16V {
   static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
-  static constexpr int kVTileBytes = 128 * 128 * 2;   // BF16 [128 keys][128 d] as two 64-channel halves
+  static constexpr int kVTileBytes = 128 * 128 * 2;
   static constexpr float kTau = 8.0f;
 };
+template <>
+struct Cfg<Mode::kSagePV16> : CfgBF16V {};
+template <>
+struct Cfg<Mode::kBF16> : CfgBF16V {};
 
-template <PV kPV>
+template <Mode kMode>
 struct __align__(1024) Smem {
-  static constexpr int kKStages = Cfg<kPV>::kKStages;
-  static constexpr int kVStages = Cfg<kPV>::kVStages;
-  uint8_t q[kNQ][kQTileBytes];
+  static constexpr int kKStages = Cfg<kMode>::kKStages;
+  static constexpr int kVStages = Cfg<kMode>::kVStages;
+  uint8_t q[kNQ][kQTileBytes];   // FP16 codes or BF16 inputs, [128 rows][64 cols] halves, 128B swizzle
   uint8_t k[kKStages][kQTileBytes];
-  uint8_t v[kVStages][Cfg<kPV>::kVTileBytes];
+  uint8_t v[kVStages][Cfg<kMode>::kVTileBytes];
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -93,12 +108,13 @@ struct __align__(1024) Smem {
   uint32_t abort_flag;
 };
 
-__device__ uint32_t g_err_sage;
+__device__ uint32_t g_err_attn;
 
 struct Params {
-  const float* q_scale;   // [B*H, nblk]
-  const float* k_scale;   // [B*H, nblk]
+  const float* q_scale;   // [B*H, nblk] (Sage modes)
+  const float* k_scale;   // [B*H, nblk] (Sage modes)
   const float* v_scale;   // [B*H, 128] (FP8 mode)
+  float c_log2;           // softmax_scale * log2 e (BF16 mode)
   __nv_bfloat16* o;
   long long o_sb, o_ss, o_sh;
   int S;
@@ -110,17 +126,18 @@ struct Params {
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
-template <PV kPV>
+template <Mode kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    sage_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  constexpr int kKStages = Cfg<kPV>::kKStages;
-  constexpr int kVStages = Cfg<kPV>::kVStages;
-  constexpr int kVTileBytes = Cfg<kPV>::kVTileBytes;
-  constexpr float kTau = Cfg<kPV>::kTau;
-  constexpr bool kFP8 = (kPV == PV::kE4M3);
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  constexpr int kKStages = Cfg<kMode>::kKStages;
+  constexpr int kVStages = Cfg<kMode>::kVStages;
+  constexpr int kVTileBytes = Cfg<kMode>::kVTileBytes;
+  constexpr float kTau = Cfg<kMode>::kTau;
+  constexpr bool kFP8 = (kMode == Mode::kSageFP8);    // P V in e4m3 (else BF16)
+  constexpr bool kInt8 = (kMode != Mode::kBF16);       // scores from the INT8 codes (else the BF16 inputs)
   extern __shared__ uint8_t smem_raw[];
-  Smem<kPV>& sm = *reinterpret_cast<Smem<kPV>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<kMode>& sm = *reinterpret_cast<Smem<kMode>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -165,25 +182,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&sm.q_full, kNQ * kQTileBytes);
       for (int i = 0; i < kNQ; ++i)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh);
+        for (int hf = 0; hf < 2; ++hf) {
+          // rows past S read as 0 (their output is not stored)
+          if constexpr (kInt8)
+            tma_load_3d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh);
+          else
+            tma_load_4d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh % p.H,
+                        bh / p.H);
+        }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
         {
           const int slot = j % kKStages, use = j / kKStages;
-          if (use > 0 && !mbar_wait<true>(&sm.k_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+          if (use > 0 && !mbar_wait<true>(&sm.k_empty[slot], (use - 1) & 1, abort_flag, &g_err_attn, kErrTimeoutSync)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&sm.k_full[slot], kQTileBytes);
-          tma_load_3d(sm.k[slot], &tm_k, &sm.k_full[slot], 0, j * kBN, bh);
-          tma_load_3d(sm.k[slot] + kHalfBytes, &tm_k, &sm.k_full[slot], 64, j * kBN, bh);
+          if constexpr (kInt8) {
+            tma_load_3d(sm.k[slot], &tm_k, &sm.k_full[slot], 0, j * kBN, bh);
+            tma_load_3d(sm.k[slot] + kHalfBytes, &tm_k, &sm.k_full[slot], 64, j * kBN, bh);
+          } else {
+            tma_load_4d(sm.k[slot], &tm_k, &sm.k_full[slot], 0, j * kBN, bh % p.H, bh / p.H);
+            tma_load_4d(sm.k[slot] + kHalfBytes, &tm_k, &sm.k_full[slot], 64, j * kBN, bh % p.H, bh / p.H);
+          }
           k_issued = j + 1;
         }
         {
           const int slot = j % kVStages, use = j / kVStages;
-          if (use > 0 && !mbar_wait<true>(&sm.v_empty[slot], (use - 1) & 1, abort_flag, &g_err_sage, kErrTimeoutSync)) {
+          if (use > 0 && !mbar_wait<true>(&sm.v_empty[slot], (use - 1) & 1, abort_flag, &g_err_attn, kErrTimeoutSync)) {
             ok = false;
             break;
           }
@@ -213,13 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lane issues every tcgen05 instruction
       const bool leader = elect_one();
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc_qk = idesc_f32acc(kFmtF16, kFmtF16, false, false, kBM, kBN);
+      const uint32_t idesc_qk = kInt8 ? idesc_f32acc(kFmtF16, kFmtF16, false, false, kBM, kBN)
+                                      : idesc_f32acc(kFmtBF16, kFmtBF16, false, false, kBM, kBN);
       const uint32_t idesc_pv = kFP8 ? idesc_f32acc(kFmtE4M3, kFmtE4M3, false, false, kBM, 128)
                                      : idesc_f32acc(kFmtBF16, kFmtBF16, false, true, kBM, 128);
       // TMEM columns of S_i and O_i
       auto tS = [&](int i) { return tmem + 128u * (uint32_t)i; };
       auto tO = [&](int i) { return tmem + 256u + 128u * (uint32_t)i; };
-      uint32_t* err = &g_err_sage;
+      uint32_t* err = &g_err_attn;
 
       auto issue_s = [&](int i, int slot) {
         const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[slot]);
@@ -305,18 +334,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + 128u * i;
     const uint32_t tO = tmem + lane_off + 256u + 128u * i;
     const int grow = q_row0 + i * kBM + row;
-    // row's Q scale (carries softmax_scale * log2 e); rows past S use block 0's slot of a real block
-    const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
-    const float qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
-    const float* ksp = p.k_scale + (long long)bh * p.nblk;
-    uint32_t* err = &g_err_sage;
+    // score factors: Sage modes, the row's Q scale (it carries softmax_scale * log2 e; rows
+    // past S use the slot of a real block) times each 32-key block's K scale; BF16 mode, c
+    float qs = p.c_log2;
+    const float* ksp = nullptr;
+    float4 ks_next = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+    if constexpr (kInt8) {
+      const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
+      qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
+      ksp = p.k_scale + (long long)bh * p.nblk;
+      ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
+    }
+    uint32_t* err = &g_err_attn;
     float m_used = -INFINITY, l = 0.0f;
     bool ok = true;
-    float4 ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
 
     for (int j = 0; j < n; ++j) {
       const float4 ks4 = ks_next;
-      if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
+      if (kInt8 && j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
       const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
       if (!mbar_wait_warp<false>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
       tc_fence_after();
@@ -507,22 +542,23 @@ __global__ void __launch_bounds__(256) widen_i8_f16_kernel(const int8_t* __restr
   }
 }
 
-template <PV kPV>
+template <Mode kMode>
 size_t smem_bytes_of() {
-  return sizeof(Smem<kPV>) + 1024;
+  return sizeof(Smem<kMode>) + 1024;
 }
 
-template <PV kPV>
-cudaError_t launch_kernel(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, const CUtensorMap& tm_v,
-                          const float* q_scale, const float* k_scale, const float* v_scale, void* o, long long o_sb,
-                          long long o_ss, long long o_sh, int B, int S, int H, long long S_pad, cudaStream_t stream) {
+template <Mode kMode>
+cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                          const float* q_scale, const float* k_scale, const float* v_scale, float c_log2, void* o,
+                          long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
+                          cudaStream_t stream) {
   static bool attr_done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  const size_t smem = smem_bytes_of<kPV>();
+  const size_t smem = smem_bytes_of<kMode>();
   if (!attr_done[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(sage_attn_kernel<kPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(attn_fwd_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -530,6 +566,7 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, 
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.c_log2 = c_log2;
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
   p.o_sb = o_sb;
   p.o_ss = o_ss;
@@ -539,13 +576,13 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16, 
   p.nblk = (int)(S_pad / 32);
   p.n_tiles = (S + kBN - 1) / kBN;
   dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
-  sage_attn_kernel<kPV><<<grid, kThreads, smem, stream>>>(tm_q16, tm_k16, tm_v, p);
+  attn_fwd_kernel<kMode><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t sage_attn_smem_bytes() { return smem_bytes_of<PV::kE4M3>(); }
+size_t sage_attn_smem_bytes() { return smem_bytes_of<Mode::kSageFP8>(); }
 
 cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,
                               int num_sms, cudaStream_t stream) {
@@ -564,23 +601,31 @@ cudaError_t launch_sage_attn(const CUtensorMap& tm_q16, const CUtensorMap& tm_k1
                              const float* q_scale, const float* k_scale, const float* v_scale, void* o,
                              long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
                              cudaStream_t stream) {
-  return launch_kernel<PV::kE4M3>(tm_q16, tm_k16, tm_v8, q_scale, k_scale, v_scale, o, o_sb, o_ss, o_sh, B, S, H,
-                                  S_pad, stream);
+  return launch_kernel<Mode::kSageFP8>(tm_q16, tm_k16, tm_v8, q_scale, k_scale, v_scale, 0.0f, o, o_sb, o_ss, o_sh,
+                                       B, S, H, S_pad, stream);
 }
 
 cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& tm_k16,
                                   const CUtensorMap& tm_v_bf16, const float* q_scale, const float* k_scale, void* o,
                                   long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
                                   long long S_pad, cudaStream_t stream) {
-  return launch_kernel<PV::kBF16>(tm_q16, tm_k16, tm_v_bf16, q_scale, k_scale, nullptr, o, o_sb, o_ss, o_sh, B, S,
-                                  H, S_pad, stream);
+  return launch_kernel<Mode::kSagePV16>(tm_q16, tm_k16, tm_v_bf16, q_scale, k_scale, nullptr, 0.0f, o, o_sb, o_ss,
+                                        o_sh, B, S, H, S_pad, stream);
 }
 
-cudaError_t read_and_clear_err_sage(uint32_t* out) {
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_err_sage, sizeof(uint32_t));
+cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
+                                 long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
+                                 cudaStream_t stream) {
+  // no prepared tensors: nblk = 1 is a placeholder, the scale pointers are not read
+  return launch_kernel<Mode::kBF16>(tm_q, tm_k, tm_v, nullptr, nullptr, nullptr, c_log2, o, o_sb, o_ss, o_sh, B, S,
+                                    H, 32, stream);
+}
+
+cudaError_t read_and_clear_err_attn(uint32_t* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_err_attn, sizeof(uint32_t));
   if (e != cudaSuccess) return e;
   const uint32_t zero = 0;
-  return cudaMemcpyToSymbol(g_err_sage, &zero, sizeof(uint32_t));
+  return cudaMemcpyToSymbol(g_err_attn, &zero, sizeof(uint32_t));
 }
 
 }  // namespace sa

@@ -11,12 +11,13 @@ namespace sa {
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// BF16 flash attention (attn_bf16.cu)
-size_t attn_bf16_smem_bytes();
-cudaError_t launch_attn_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
-                             long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
-                             cudaStream_t stream);
-cudaError_t read_and_clear_err_bf16(uint32_t* out);
+// The attention forward kernel, three modes (attn_fwd.cu).  BF16 flash attention:
+// Q, K, V through [B, S, H, 128] BF16 tensor maps.
+cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
+                                 long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
+                                 cudaStream_t stream);
+// The device error word all three modes record bounded-wait timeouts in.
+cudaError_t read_and_clear_err_attn(uint32_t* out);
 
 // Sage prepare (sage_prepare.cu)
 struct PrepareArgs {
@@ -48,7 +49,7 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 constexpr int kNoAllocMaxHeads = 2048;
 cudaError_t noalloc_prepare_scratch(uint32_t** out);
 
-// Sage attention on prepared tensors (sage_attn.cu)
+// Sage attention on prepared tensors (attn_fwd.cu)
 size_t sage_attn_smem_bytes();
 cudaError_t launch_sage_widen(const int8_t* q8, const int8_t* k8, void* q16, void* k16, long long n_codes,
                               int num_sms, cudaStream_t stream);
@@ -61,6 +62,5 @@ cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& 
                                   const CUtensorMap& tm_v_bf16, const float* q_scale, const float* k_scale, void* o,
                                   long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
                                   long long S_pad, cudaStream_t stream);
-cudaError_t read_and_clear_err_sage(uint32_t* out);
 
 }  // namespace sa
