@@ -264,6 +264,23 @@ ATTN_API attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, 
  */
 ATTN_API attn_status attn_get_device_status(attn_stream_t stream);
 
+/*
+ * attn_selftest_wait_timeout -- exercises the failure path described above on
+ * this GPU.  It launches the BF16 attention kernel on a [1, 128, 1, 128] problem
+ * with its tile loads withheld, so that the MMA warp's first wait (for Q) runs
+ * out after the kernels' wait limit (2 s of %globaltimer); the kernel then
+ * raises its abort flag, the other roles leave their loops, TMEM is freed and
+ * the kernel returns.  The call synchronises `stream` and returns what
+ * attn_get_device_status reports for that launch: ATTN_ERR_DEVICE_TIMEOUT when
+ * the failure path works.  The context stays usable afterwards.
+ *   q, k, v, o : BF16 [1, 128, 1, 128] contiguous device buffers (nothing is read
+ *                from q, k, v; o is not written)
+ * Takes about 2 s.  Errors: bad pointers -> ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_ALIGNMENT; not an sm_103 device -> ATTN_ERR_UNSUPPORTED.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(const void* q, const void* k, const void* v, void* o,
+                                                attn_stream_t stream);
+
 /* attn_last_error -- message of the calling thread's last failed call ("" if none). */
 ATTN_API const char* attn_last_error(void);
 

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.sage_attn_fwd_pv16.argtypes = [_vp, _vp, _vp, _vp, _vp, _I64x3, _vp, _I64x3, i, i, i, i, ctypes.c_int64,
                                          _vp, ctypes.c_size_t, _vp]
         L.sage_attn_fwd_pv16.restype = i
+        L.attn_selftest_wait_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp]
+        L.attn_selftest_wait_timeout.restype = i
         L.attn_get_device_status.argtypes = [_vp]
         L.attn_get_device_status.restype = i
         L.attn_last_error.argtypes = []
@@ -285,6 +287,16 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
     if pv == "bf16":
         return sage_attn_fwd_pv16(prep, v, out=out, stream=stream)
     return sage_attn_fwd(prep, out=out, stream=stream)
+
+
+def attn_selftest_wait_timeout(device=None, stream=None) -> str:
+    """Run the library's failure-path self-test on `device` (about 2 s): a kernel
+    whose loads are withheld must give up on its bounded wait and report it.
+    Returns the status name; "ATTN_ERR_DEVICE_TIMEOUT" means the path works."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    bufs = [torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    code = lib().attn_selftest_wait_timeout(*(b.data_ptr() for b in bufs), _stream_ptr(stream))
+    return STATUS.get(code, str(code))
 
 
 def attn_get_device_status(stream=None) -> None:

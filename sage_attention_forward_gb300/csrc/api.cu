@@ -469,6 +469,30 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
   return ATTN_OK;
 }
 
+attn_status attn_selftest_wait_timeout(const void* q, const void* k, const void* v, void* o,
+                                       attn_stream_t stream) {
+  const int64_t st[3] = {128 * 128, 128, 128};   // [1, 128, 1, 128] contiguous
+  long long qs[3], ks[3], vs[3], os[3];
+  TRY(check_strides("q", q, st, 1, 128, 1, qs));
+  TRY(check_strides("k", k, st, 1, 128, 1, ks));
+  TRY(check_strides("v", v, st, 1, 128, 1, vs));
+  TRY(check_strides("o", o, st, 1, 128, 1, os));
+  TRY(check_device());
+  TRY(get_encoder());
+  // start from a clean error word, so that the status below is this launch's
+  attn_status pre = attn_get_device_status(stream);
+  if (pre != ATTN_OK && pre != ATTN_ERR_DEVICE_TIMEOUT) return pre;
+  CUtensorMap tq, tk, tv;
+  TRY(tmap_bhsd_bf16(&tq, q, 1, 128, 1, qs));
+  TRY(tmap_bhsd_bf16(&tk, k, 1, 128, 1, ks));
+  TRY(tmap_bhsd_bf16(&tv, v, 1, 128, 1, vs));
+  const float c = (float)(0.08838834764831845 * kLog2e);
+  cudaError_t e = sa::launch_attn_fwd_bf16(tq, tk, tv, o, os[0], os[1], os[2], 1, 128, 1, c, (cudaStream_t)stream,
+                                           /*withhold_loads=*/true);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_selftest_wait_timeout launch");
+  return attn_get_device_status(stream);
+}
+
 attn_status attn_get_device_status(attn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");

@@ -121,6 +121,7 @@ struct Params {
   int H;
   int nblk;               // S_pad / 32
   int n_tiles;            // ceil(S / 128)
+  int withhold_loads;     // self-test of the failure path: the producer loads nothing
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -175,7 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == kWarpLoad) {
-    if (lane == 0) {
+    // with withhold_loads set (attn_selftest_wait_timeout) nothing is loaded: the MMA warp's
+    // wait for Q runs out, and the kernel must still return with the timeout recorded
+    if (lane == 0 && !p.withhold_loads) {
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -551,7 +554,7 @@ template <Mode kMode>
 cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const float* q_scale, const float* k_scale, const float* v_scale, float c_log2, void* o,
                           long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool withhold_loads = false) {
   static bool attr_done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
@@ -575,6 +578,7 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   p.H = H;
   p.nblk = (int)(S_pad / 32);
   p.n_tiles = (S + kBN - 1) / kBN;
+  p.withhold_loads = withhold_loads ? 1 : 0;
   dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
   attn_fwd_kernel<kMode><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
@@ -615,10 +619,10 @@ cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& 
 
 cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                                  long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool withhold_loads) {
   // no prepared tensors: nblk = 1 is a placeholder, the scale pointers are not read
   return launch_kernel<Mode::kBF16>(tm_q, tm_k, tm_v, nullptr, nullptr, nullptr, c_log2, o, o_sb, o_ss, o_sh, B, S,
-                                    H, 32, stream);
+                                    H, 32, stream, withhold_loads);
 }
 
 cudaError_t read_and_clear_err_attn(uint32_t* out) {

@@ -13,9 +13,10 @@ int device_sm_count();
 
 // The attention forward kernel, three modes (attn_fwd.cu).  BF16 flash attention:
 // Q, K, V through [B, S, H, 128] BF16 tensor maps.
+// withhold_loads: the failure-path self-test (the producer loads nothing).
 cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                                  long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool withhold_loads = false);
 // The device error word all three modes record bounded-wait timeouts in.
 cudaError_t read_and_clear_err_attn(uint32_t* out);
 

@@ -132,6 +132,12 @@ def test_sage_attn_fwd_pv16_rejects_bad_arguments():
     assert call(D=64) == 3
 
 
+def test_selftest_rejects_bad_pointers():
+    L = sa.lib()
+    assert L.attn_selftest_wait_timeout(None, FAKE, FAKE, FAKE, None) == 1
+    assert L.attn_selftest_wait_timeout(FAKE, FAKE, FAKE, FAKE + 8, None) == 2
+
+
 def test_product_path_does_not_import_the_oracle():
     import subprocess
     import sys
