@@ -242,7 +242,7 @@ ATTN_API attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const
  * accuracy: V is not quantised and P carries 8 significant bits instead of 4.
  *   O[r, d] = sum_j p[r, j] v[j, d] / sum_j p[r, j],  p = bf16(2^(t - m_r)),
  *   t as in sage_attn_fwd, m_r the row's reference maximum (moved only when a
- *   tile's maximum passes it by more than 8 log2 units), the denominator summed
+ *   tile's maximum passes it by more than 32 log2 units), the denominator summed
  *   from the unrounded p in FP32.
  *   q_i8, k_i8, q_scale, k_scale : from sage_prepare or sage_prepare_smooth_k
  *                (its v_fp8 / v_scale outputs are not read)

@@ -83,7 +83,9 @@ struct CfgBF16V {
   static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   static constexpr int kVTileBytes = 128 * 128 * 2;
-  static constexpr float kTau = 8.0f;
+  // BF16 keeps FP32's exponent range, so the reference may lag far: p <= 2^32 stays
+  // exact to BF16 precision and the FP32 sums cannot overflow, and O is rescaled rarely
+  static constexpr float kTau = 32.0f;
 };
 template <>
 struct Cfg<Mode::kSagePV16> : CfgBF16V {};
@@ -450,14 +452,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               // before the first half of P_j V_j accumulates into it
               if (mbar_wait_warp<true>(&sm.o_done[i], (j - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
                 tc_fence_after();
+                // O_i *= sc in 16-column chunks, the next chunk's load in flight while this
+                // one is scaled and stored
+                uint32_t oa[16], ob[16];
+                tmem_ld16(tO, oa);
+                tmem_ld_wait();
+                tmem_reg_fence16(oa);
 #pragma unroll
-                for (int c2 = 0; c2 < 8; ++c2) {
-                  uint32_t o[16];
-                  tmem_ld16(tO + 16 * c2, o);
+                for (int c2 = 0; c2 < 8; c2 += 2) {
+                  tmem_ld16(tO + 16 * (c2 + 1), ob);
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) oa[e] = f2u(u2f(oa[e]) * sc);
+                  tmem_st16(tO + 16 * c2, oa);
                   tmem_ld_wait();
+                  tmem_reg_fence16(ob);
+                  if (c2 + 2 < 8) tmem_ld16(tO + 16 * (c2 + 2), oa);
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) o[e] = f2u(u2f(o[e]) * sc);
-                  tmem_st16(tO + 16 * c2, o);
+                  for (int e = 0; e < 16; ++e) ob[e] = f2u(u2f(ob[e]) * sc);
+                  tmem_st16(tO + 16 * (c2 + 1), ob);
+                  if (c2 + 2 < 8) {
+                    tmem_ld_wait();
+                    tmem_reg_fence16(oa);
+                  }
                 }
               } else {
                 ok = false;
@@ -489,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         tmem_ld32(tO + 32 * cc, o);
         tmem_ld_wait();
+        tmem_reg_fence(o);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
