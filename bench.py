@@ -56,6 +56,15 @@ def kernel_traffic(record: str, workload: str):
     return rec["dram_bytes_per_launch_wan720p_scaled"]
 
 
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of the JSON line; both arms report the same one."""
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} S={wl.S} D={wl.D}"
+                        + (", 5% outlier tokens x8" if wl.outlier_frac else ""),
+            "B": wl.B, "H": wl.H, "S": wl.S, "D": wl.D,
+            "step": "attn_fwd_bf16 + sage_prepare + sage_attn_fwd (two attention evaluations)",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -271,11 +280,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16+int8/e4m3",
         "data": "synthetic",
-        "config": {"workload": f"{wl.name}: B={B} H={H} S={S} D={D}"
-                               + (", 5% outlier tokens x8" if wl.outlier_frac else ""),
-                   "B": B, "H": H, "S": S, "D": D,
-                   "step": "attn_fwd_bf16 + sage_prepare + sage_attn_fwd (two attention evaluations)",
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "config": workload_config(wl, world),
         "providers": providers,
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": roof_tflops,
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
@@ -393,8 +398,7 @@ def run_reference(args, rank, world):
     return {"metric": METRIC, "value": value, "unit": "TFLOPS", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} S={wl.S} D={wl.D}", "B": wl.B, "H": wl.H,
-                       "S": wl.S, "D": wl.D, "step": "CPU oracle, FP64 attention on sampled query rows"},
+            "config": workload_config(wl, world),
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
