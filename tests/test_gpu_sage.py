@@ -124,3 +124,22 @@ def test_forward_on_oracle_prepared_tensors(cuda_dev):
 
 def test_device_status_is_clean(cuda_dev):
     sa.attn_get_device_status()
+
+
+def test_permuted_output_layout_both_modes(cuda_dev, workload_inputs):
+    """HunyuanVideo's head-major storage for the output as well as the inputs: both
+    Sage modes write the [B, H, S, D] buffer seen as [B, S, H, D] exactly as they
+    write a contiguous output."""
+    cpu, g = workload_inputs("hunyuan720p")
+    B, S, H, D = g.q.shape
+    prep = sa.sage_prepare(g.q, g.k, g.v, softmax_scale=cpu.wl.softmax_scale)
+    for fwd in (lambda out=None: sa.sage_attn_fwd(prep, out=out),
+                lambda out=None: sa.sage_attn_fwd_pv16(prep, g.v, out=out)):
+        o_contig = fwd()
+        o_store = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=cuda_dev)
+        o_perm = o_store.permute(0, 2, 1, 3)
+        fwd(out=o_perm)
+        torch.cuda.synchronize()
+        assert torch.equal(o_perm, o_contig)
+        del o_contig, o_store, o_perm
+    sa.attn_get_device_status()
