@@ -255,13 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto tO = [&](int i) { return tmem + 256u + 128u * (uint32_t)i; };
       uint32_t* err = &g_err_attn;
 
+      // shared-memory descriptors: the base once, then the step offsets (in 16-byte units)
+      // added to the address field, which cannot carry out for addresses below 256 KB
+      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t qdesc1 = smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024);
       auto issue_s = [&](int i, int slot) {
-        const uint32_t qa = smem_u32(sm.q[i]), ka = smem_u32(sm.k[slot]);
+        const uint64_t qd = i == 0 ? qdesc0 : qdesc1, kd = smem_desc_sw128(smem_u32(sm.k[slot]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          const uint64_t da = smem_desc_sw128(qa + off, 16, 1024), db = smem_desc_sw128(ka + off, 16, 1024);
-          if (leader) mma_f16_ss(tS(i), da, db, idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          if (leader) mma_f16_ss(tS(i), qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       // O_i += P_i V for keys [64*half, 64*half + 64).  FP8: 2 steps of 32 positions
@@ -271,18 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv_half = [&](int i, int slot, int half, bool acc) {
         const uint32_t va = smem_u32(sm.v[slot]);
         if constexpr (kFP8) {
+          const uint64_t vd = smem_desc_sw128(va, 16, 1024);
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             const int kk = 2 * half + k2;
-            const uint64_t db = smem_desc_sw128(va + kk * 32, 16, 1024);
-            if (leader) mma_f8_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            if (leader) mma_f8_ts(tO(i), tS(i) + kk * 8, vd + ((kk * 32) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
           }
         } else {
+          const uint64_t vd = smem_desc_sw128(va, kHalfBytes, 1024);
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = 4 * half + k4;
-            const uint64_t db = smem_desc_sw128(va + kk * 2048, kHalfBytes, 1024);
-            if (leader) mma_f16_ts(tO(i), tS(i) + kk * 8, db, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            if (leader) mma_f16_ts(tO(i), tS(i) + kk * 8, vd + ((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
           }
         }
       };
@@ -307,24 +310,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) mma_commit(&sm.s_full[1]);
         if (leader) mma_commit(&sm.k_empty[0]);
       }
-      for (int j = 0; j < n && ok; ++j) {
-        const int slotV = j % kVStages;
-        const int slotK = (j + 1) % kKStages;
-        const bool more = (j + 1 < n);
-        if (!mbar_wait_warp<false>(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
-        if (!issue_pv(0, slotV, j)) break;
-        if (more) {
-          if (!mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) break;
-          tc_fence_after();
-          issue_s(0, slotK);
-          if (leader) mma_commit(&sm.s_full[0]);
-        }
-        if (!issue_pv(1, slotV, j)) break;
-        if (leader) mma_commit(&sm.v_empty[slotV]);
-        if (more) {
-          issue_s(1, slotK);
-          if (leader) mma_commit(&sm.s_full[1]);
-          if (leader) mma_commit(&sm.k_empty[slotK]);
+      // unrolled by the ring depth, so that every ring slot (and with it every shared-memory
+      // descriptor) is a compile-time constant of its copy of the body
+      static_assert(kKStages == kVStages, "one ring depth for K and V");
+      for (int j0 = 0; j0 < n && ok; j0 += kKStages) {
+#pragma unroll
+        for (int u = 0; u < kKStages; ++u) {
+          const int j = j0 + u;
+          if (j >= n || !ok) break;
+          const int slotV = u;
+          const int slotK = (u + 1) % kKStages;
+          const bool more = (j + 1 < n);
+          if (!mbar_wait_warp<false>(&sm.v_full[slotV], (j / kVStages) & 1, abort_flag, err, kErrTimeoutTma)) {
+            ok = false;
+            break;
+          }
+          if (!issue_pv(0, slotV, j)) { ok = false; break; }
+          if (more) {
+            if (!mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
+                                       kErrTimeoutTma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, slotK);
+            if (leader) mma_commit(&sm.s_full[0]);
+          }
+          if (!issue_pv(1, slotV, j)) { ok = false; break; }
+          if (leader) mma_commit(&sm.v_empty[slotV]);
+          if (more) {
+            issue_s(1, slotK);
+            if (leader) mma_commit(&sm.s_full[1]);
+            if (leader) mma_commit(&sm.k_empty[slotK]);
+          }
         }
       }
       if (leader) mma_commit(&sm.mma_drain);
