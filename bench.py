@@ -56,6 +56,31 @@ def kernel_traffic(record: str, workload: str):
     return rec["dram_bytes_per_launch_wan720p_scaled"]
 
 
+# ----------------------------------------------------------------------------- ranks
+# One process per GPU (torchrun).  Ranks are independent replicas: nothing crosses
+# between them but the barrier around the timed region and the maximum of the ranks'
+# times, which these helpers carry (NCCL on the GPU path; any backend works).
+def rank_info() -> tuple:
+    """(rank, world size, local rank) from the launcher's environment (1 process if unset)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: the whole job finishes when its last replica does."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Work of all ranks (each runs the full step) over the slowest rank's time, in TFLOPS."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def workload_config(wl, world: int) -> dict:
     """The `config` object of the JSON line; both arms report the same one."""
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} S={wl.S} D={wl.D}"
@@ -190,11 +215,7 @@ def run_ours(args, rank, world):
         t_end.record(stream)
         barrier()
     sa.attn_get_device_status()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
 
     # the step's own split (each call timed inside the interleaved step)
     per = {"bf16": [], "prepare": [], "sage_core": []}
@@ -269,7 +290,7 @@ def run_ours(args, rank, world):
 
     result = {
         "metric": METRIC,
-        "value": world * 2 * F * args.steps / (elapsed_ms * 1e-3) / 1e12,
+        "value": whole_job_tflops(world, 2 * F, args.steps, elapsed_ms),
         "unit": "TFLOPS",
         "n_gpus": world,
         "steps": args.steps,
@@ -362,14 +383,10 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
     t1.record(comp)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
-    ms = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     in_bytes = 3 * hq.numel() * 2
     out_bytes = 2 * ho1.numel() * 2
-    return {"value": world * 2 * F * steps / (ms * 1e-3) / 1e12, "unit": "TFLOPS",
+    return {"value": whole_job_tflops(world, 2 * F, steps, ms), "unit": "TFLOPS",
             "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "steps": steps,
             "ms_per_step": ms / steps,
             "overlap": "H2D, compute and D2H of consecutive steps on three streams, double-buffered device "
@@ -446,8 +463,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    rank, world, local_rank = rank_info()
     if args.impl == "reference":
         if rank != 0:
             return
@@ -456,7 +472,7 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     res = run_ours(args, rank, world)
     if rank == 0:
