@@ -26,7 +26,9 @@
  *                   prepared tensors".)
  *
  * Conventions shared by every call
- *   - D (head dimension) must be 128; B, S, H >= 1.
+ *   - D (head dimension) must be 128; S >= 1 (attention over no keys is undefined:
+ *     S = 0 is ATTN_ERR_INVALID_ARG).  B = 0 or H = 0 is an empty problem: every call
+ *     returns ATTN_OK at once, writing and reading nothing (its pointers may be NULL).
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
  *     owned by the caller; the library never allocates, frees or keeps them.
  *     Every pointer must be 16-byte aligned.

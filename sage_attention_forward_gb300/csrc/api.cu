@@ -120,9 +120,18 @@ attn_status tmap_bytes_3d(CUtensorMap* m, const void* ptr, long long n0, long lo
 // ------------------------------------------------------------------ validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-attn_status check_shape(int B, int S, int H, int D) {
+// B = 0 or H = 0 (no query rows at all) is a valid empty problem: *empty is set and the
+// caller returns ATTN_OK without touching its pointers.  S = 0 is an error: attention over
+// no keys is undefined.
+attn_status check_shape(int B, int S, int H, int D, bool* empty) {
+  *empty = false;
   if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dimension D=%d; only D=128 is supported", D);
-  if (B < 1 || S < 1 || H < 1) return fail(ATTN_ERR_INVALID_ARG, "B=%d S=%d H=%d must all be >= 1", B, S, H);
+  if (B < 0 || H < 0) return fail(ATTN_ERR_INVALID_ARG, "B=%d H=%d must be >= 0", B, H);
+  if (S < 1) return fail(ATTN_ERR_INVALID_ARG, "S=%d: attention needs at least one key (S >= 1)", S);
+  if (B == 0 || H == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
   if (B > 65535 || H > 65535 || (long long)B * H > 65535)
     return fail(ATTN_ERR_INVALID_ARG, "B=%d H=%d: B*H must be <= 65535", B, H);
   return ATTN_OK;
@@ -180,7 +189,9 @@ extern "C" {
 attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, int B, int S, int H, int D,
                           const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                           const int64_t o_str[3], float softmax_scale, attn_stream_t stream) {
-  TRY(check_shape(B, S, H, D));
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   long long qs[3], ks[3], vs[3], os[3];
   TRY(check_strides("q", q, q_str, B, S, H, qs));
   TRY(check_strides("k", k, k_str, B, S, H, ks));
@@ -205,7 +216,9 @@ attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, in
                                  const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
                                  int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
                                  float* v_scale, attn_stream_t stream) {
-  TRY(check_shape(B, S, H, D));
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   if ((long long)B * H > sa::kNoAllocMaxHeads)
     return fail(ATTN_ERR_INVALID_ARG,
                 "sage_prepare_noalloc: B*H=%lld heads exceeds the %d heads its static scratch holds; use "
@@ -285,7 +298,9 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
                          int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
                          void* workspace, size_t workspace_bytes, size_t workspace_needed, float* k_mean,
                          attn_stream_t stream) {
-  TRY(check_shape(B, S, H, D));
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   sa::PrepareArgs a;
   TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
   TRY(check_strides("k", k, k_str, B, S, H, a.str[1]));
@@ -376,6 +391,9 @@ attn_status sage_prepare_smooth_k(const void* q, const void* k, const void* v, i
                                   int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
                                   float* v_scale, float* k_mean, void* workspace, size_t workspace_bytes,
                                   attn_stream_t stream) {
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   if (k_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "sage_prepare_smooth_k: k_mean is NULL");
   if (!aligned16(k_mean)) return fail(ATTN_ERR_ALIGNMENT, "sage_prepare_smooth_k: k_mean is not 16-byte aligned");
   return prepare_checked("sage_prepare_smooth_k", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale,
@@ -393,7 +411,9 @@ attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t*
                           const float* k_scale, const float* v_scale, void* o, const int64_t o_str[3], int B,
                           int S, int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
                           attn_stream_t stream) {
-  TRY(check_shape(B, S, H, D));
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   if (S_pad < S || S_pad % 128 != 0)
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
@@ -433,7 +453,9 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
                                const void* v, const int64_t v_str[3], void* o, const int64_t o_str[3], int B, int S,
                                int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
                                attn_stream_t stream) {
-  TRY(check_shape(B, S, H, D));
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
   if (S_pad < S || S_pad % 128 != 0)
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);

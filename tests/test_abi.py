@@ -48,8 +48,9 @@ def call_fwd(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, S=256, H=2, D=128, qs=(256 * 2
 
 @pytest.mark.parametrize("kw,status", [
     (dict(D=64), 3),
-    (dict(B=0), 1),
-    (dict(S=0), 1),
+    (dict(B=0), 0),                    # no query rows: an empty problem, nothing happens
+    (dict(H=0, q=0, k=0, v=0, o=0), 0),   # ... and its pointers are not looked at
+    (dict(S=0), 1),                    # no keys: attention is undefined
     (dict(H=-1), 1),
     (dict(q=0), 1),
     (dict(o=FAKE + 8), 2),
@@ -60,7 +61,8 @@ def call_fwd(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, S=256, H=2, D=128, qs=(256 * 2
 ])
 def test_attn_fwd_bf16_rejects_bad_arguments(kw, status):
     assert call_fwd(**kw) == status
-    assert sa.lib().attn_last_error().decode() != ""
+    if status:
+        assert sa.lib().attn_last_error().decode() != ""
 
 
 def call_prepare(rope_dim=0, S_pad=256, qn=None, kn=None, ws_bytes=10**6, cos=None):
