@@ -325,9 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // with a three-deep K ring the next K tile is resident by now: waiting for it here
+          // takes that wait off the path from P_0 V_j to S_0(j+1); with two stages it often
+          // is not yet, and the wait stays where S_0 needs it
+          constexpr bool kEarlyK = (kKStages >= 3);
+          if (kEarlyK && more &&
+              !mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
+                                     kErrTimeoutTma)) {
+            ok = false;
+            break;
+          }
           if (!issue_pv(0, slotV, j)) { ok = false; break; }
           if (more) {
-            if (!mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
+            if (!kEarlyK &&
+                !mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
                                        kErrTimeoutTma)) {
               ok = false;
               break;
