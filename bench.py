@@ -34,7 +34,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention TFLOPS (4·B·H·S²·D/s) at S=76112,H=40,D=128; % of tensor peak"
-KERNELS_PER_STEP = 5  # attn_bf16, prep_qk_vmax, prep_v, widen_i8_f16, sage_attn
+KERNELS_PER_STEP = 4  # attn_fwd (BF16), prep_qk_vmax, prep_v, attn_fwd (Sage FP8)
 
 
 def kernel_traffic(record: str, workload: str):
@@ -86,7 +86,7 @@ def workload_config(wl, world: int) -> dict:
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} S={wl.S} D={wl.D}"
                         + (", 5% outlier tokens x8" if wl.outlier_frac else ""),
             "B": wl.B, "H": wl.H, "S": wl.S, "D": wl.D,
-            "step": "attn_fwd_bf16 + sage_prepare + sage_attn_fwd (two attention evaluations)",
+            "step": "attn_fwd_bf16 + sage_attention (prepare + forward in one call; two attention evaluations)",
             "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
 
 
@@ -170,6 +170,7 @@ def run_ours(args, rank, world):
     prep = sa.Prepared.empty(B, H, S, S_pad, dev)
     ws_p = sa.prepare_workspace(B, H, dev)
     ws_a = sa.attn_workspace(B, H, S_pad, dev)
+    ws_1 = sa.sage_attention_workspace(B, H, S, dev)
     kw = {}
     if inp.q_norm_w is not None:
         kw.update(q_norm_w=inp.q_norm_w, k_norm_w=inp.k_norm_w, rms_eps=wl.rms_eps)
@@ -183,12 +184,9 @@ def run_ours(args, rank, world):
         sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale)
         if ev is not None:
             ev[1].record(stream)
-        sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw)
+        sa.sage_attention(q, k, v, softmax_scale=scale, out=o_sage, workspace=ws_1, **kw)
         if ev is not None:
             ev[2].record(stream)
-        sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)
-        if ev is not None:
-            ev[3].record(stream)
 
     dist = None
     if world > 1:
@@ -205,7 +203,7 @@ def run_ours(args, rank, world):
     sa.attn_get_device_status()
     barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
         barrier()
@@ -218,11 +216,10 @@ def run_ours(args, rank, world):
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
 
     # the step's own split (each call timed inside the interleaved step)
-    per = {"bf16": [], "prepare": [], "sage_core": []}
+    per = {"bf16": [], "sage": []}
     for e in evs:
         per["bf16"].append(e[0].elapsed_time(e[1]))
-        per["prepare"].append(e[1].elapsed_time(e[2]))
-        per["sage_core"].append(e[2].elapsed_time(e[3]))
+        per["sage"].append(e[1].elapsed_time(e[2]))
     F = roofline.attention_flops(B, H, S, D)
     step_ms = {k2: statistics.mean(v2) for k2, v2 in per.items()}
     peaks = load_peaks()
@@ -233,10 +230,16 @@ def run_ours(args, rank, world):
     o_pv16 = torch.empty_like(o_bf16)
     prep_s = sa.Prepared.empty(B, H, S, S_pad, dev)
     ws_s = sa.prepare_workspace(B, H, dev, S_pad, smooth_k=True)
+    ws_16 = sa.sage_attention_workspace(B, H, S, dev, pv="bf16")
+    sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw)
     calls = {
         "bf16": lambda: sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale),
-        "sage": lambda: (sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw),
-                         sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)),
+        "sage": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_sage, workspace=ws_1, **kw),
+        "sage_two_calls": lambda: (sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep,
+                                                   workspace=ws_p, **kw),
+                                   sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)),
+        "sage_pv16": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_pv16, workspace=ws_16, pv="bf16",
+                                               **kw),
         "sage_core": lambda: sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a),
         "sage_pv16_core": lambda: sa.sage_attn_fwd_pv16(prep, v, out=o_pv16, workspace=ws_a),
         "prepare": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p,
@@ -269,7 +272,10 @@ def run_ours(args, rank, world):
     roof_tflops = F / (step_ms["bf16"] * 1e-3) / 1e12
     providers = {
         "bf16": {"ms": ms["bf16"], "tflops": bf16_tflops},
-        "sage": {"ms": ms["sage"], "tflops": tf("sage")},
+        "sage": {"ms": ms["sage"], "tflops": tf("sage"), "call": "sage_attention (prepare + forward, one call)"},
+        "sage_two_calls": {"ms": ms["sage_two_calls"], "tflops": tf("sage_two_calls"),
+                           "call": "sage_prepare, then sage_attn_fwd"},
+        "sage_pv16": {"ms": ms["sage_pv16"], "tflops": tf("sage_pv16"), "call": "sage_attention(pv=bf16)"},
         "sage_core": {"ms": ms["sage_core"], "tflops": tf("sage_core"),
                       # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
                       "frac_of_tensor_roof": tf("sage_core") / (peaks["bf16_sustained"] / 0.75)},
@@ -283,7 +289,7 @@ def run_ours(args, rank, world):
         "timing": "each provider alone: 2 warm-up + 5 calls, 3 interleaved rounds, median",
         "in_step_ms": step_ms,
     }
-    del prep_s, ws_s, o_pv16
+    del prep_s, ws_s, o_pv16, ws_16
 
     # ------------------------------------------------------------- end to end
     e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)
@@ -332,9 +338,7 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
     shape = (B, S, H, D)
     din = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3)] for _ in range(2)]
     dout = [[torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)] for _ in range(2)]
-    prep = sa.Prepared.empty(B, H, S, S_pad, dev)
-    ws_p = sa.prepare_workspace(B, H, dev)
-    ws_a = sa.attn_workspace(B, H, S_pad, dev)
+    ws_1 = sa.sage_attention_workspace(B, H, S, dev)
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -356,9 +360,7 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
             if i >= 2:
                 comp.wait_event(out_done[bf])         # step i-2's outputs have left these buffers
             sa.attn_fwd_bf16(dq, dk, dv, out=o1, softmax_scale=scale, stream=comp)
-            sa.sage_prepare(dq, dk, dv, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, stream=comp,
-                            **kw)
-            sa.sage_attn_fwd(prep, out=o2, workspace=ws_a, stream=comp)
+            sa.sage_attention(dq, dk, dv, softmax_scale=scale, out=o2, workspace=ws_1, stream=comp, **kw)
             comp_done[bf].record(comp)
             s_out.wait_event(comp_done[bf])
             with torch.cuda.stream(s_out):

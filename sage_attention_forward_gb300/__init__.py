@@ -80,6 +80,11 @@ def lib() -> ctypes.CDLL:
         L.sage_attn_fwd_pv16.argtypes = [_vp, _vp, _vp, _vp, _vp, _I64x3, _vp, _I64x3, i, i, i, i, ctypes.c_int64,
                                          _vp, ctypes.c_size_t, _vp]
         L.sage_attn_fwd_pv16.restype = i
+        L.sage_attention_workspace_size.argtypes = [i, i, ctypes.c_int64, i, i]
+        L.sage_attention_workspace_size.restype = ctypes.c_size_t
+        L.sage_attention.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp, _vp,
+                                     ctypes.c_float, _vp, _vp, i, i, i, _vp, _I64x3, _vp, ctypes.c_size_t, _vp]
+        L.sage_attention.restype = i
         L.attn_selftest_wait_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.attn_selftest_wait_timeout.restype = i
         L.attn_get_device_status.argtypes = [_vp]
@@ -274,19 +279,37 @@ def sage_attn_fwd_pv16(prep: Prepared, v: torch.Tensor, out: torch.Tensor | None
     return out
 
 
-def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
-                   rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3") -> torch.Tensor:
-    """Prepare + attention: the SageAttention-style forward of BF16 Q/K/V.
+def sage_attention_workspace(B: int, H: int, S: int, device, smooth_k: bool = False, pv: str = "e4m3") -> torch.Tensor:
+    n = int(lib().sage_attention_workspace_size(B, H, sage_padded_len(S), int(smooth_k), int(pv == "bf16")))
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
-    pv="e4m3": P and V in FP8 (sage_attn_fwd); pv="bf16": P in BF16 times the
-    unquantised V (sage_attn_fwd_pv16)."""
+
+def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
+                   rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3",
+                   workspace=None) -> torch.Tensor:
+    """Prepare + attention in one library call: the SageAttention-style forward of BF16 Q/K/V.
+
+    pv="e4m3": P and V in FP8; pv="bf16": P in BF16 times the unquantised V.  The
+    prepared tensors stay in `workspace` (allocated here unless given)."""
     if pv not in ("e4m3", "bf16"):
         raise ValueError(f"pv must be 'e4m3' or 'bf16', not {pv!r}")
-    prep = sage_prepare(q, k, v, softmax_scale, None, q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim,
-                        stream=stream, smooth_k=smooth_k)
-    if pv == "bf16":
-        return sage_attn_fwd_pv16(prep, v, out=out, stream=stream)
-    return sage_attn_fwd(prep, out=out, stream=stream)
+    B, S, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = sage_attention_workspace(B, H, S, q.device, smooth_k, pv)
+    qs, ks, vs, os_ = _bshd("q", q), _bshd("k", k), _bshd("v", v), _bshd("out", out)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    _check(lib().sage_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
+                                float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
+                                ptr(rope_sin), int(rope_dim), int(bool(smooth_k)), int(pv == "bf16"),
+                                out.data_ptr(), os_, workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+    return out
 
 
 def attn_selftest_wait_timeout(device=None, stream=None) -> str:

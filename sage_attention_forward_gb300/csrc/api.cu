@@ -291,17 +291,13 @@ size_t sage_prepare_workspace_size(int B, int H) {
   return (size_t)B * (size_t)H * 128 * sizeof(uint32_t);
 }
 
-static attn_status prepare_checked(const char* who, const void* q, const void* k, const void* v, int B, int S, int H, int D,
-                         const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
-                         float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
-                         const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
-                         int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
-                         void* workspace, size_t workspace_bytes, size_t workspace_needed, float* k_mean,
-                         attn_stream_t stream) {
-  bool empty = false;
-  TRY(check_shape(B, S, H, D, &empty));
-  if (empty) return ATTN_OK;
-  sa::PrepareArgs a;
+// Inputs and options of the prepare stage (shape already checked, not empty): strides,
+// softmax scale, S_pad, RMSNorm and RoPE arguments; fills the input side of `a`.
+static attn_status prepare_inputs(const void* q, const void* k, const void* v, int B, int S, int H,
+                                  const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                  float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                  const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                  sa::PrepareArgs& a) {
   TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
   TRY(check_strides("k", k, k_str, B, S, H, a.str[1]));
   TRY(check_strides("v", v, v_str, B, S, H, a.str[2]));
@@ -322,19 +318,6 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
     if (!aligned16(rope_cos) || !aligned16(rope_sin))
       return fail(ATTN_ERR_ALIGNMENT, "RoPE tables must be 16-byte aligned");
   }
-  struct {
-    const char* n;
-    const void* p;
-  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale},
-              {"k_scale", k_scale}, {"v_scale", v_scale}, {"workspace", workspace}};
-  for (auto& t : outs) {
-    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
-    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
-  }
-  if (workspace_bytes < workspace_needed)
-    return fail(ATTN_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu required", who, workspace_bytes,
-                workspace_needed);
-  TRY(check_device());
   a.x[0] = q;
   a.x[1] = k;
   a.x[2] = v;
@@ -348,13 +331,42 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
   a.rope_cos = rope_dim > 0 ? rope_cos : nullptr;
   a.rope_sin = rope_dim > 0 ? rope_sin : nullptr;
   a.rope_dim = rope_dim;
+  a.c_log2 = (float)((double)softmax_scale * kLog2e);
+  return ATTN_OK;
+}
+
+static attn_status prepare_checked(const char* who, const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                         const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                         float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                         const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
+                         int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
+                         void* workspace, size_t workspace_bytes, size_t workspace_needed, float* k_mean,
+                         attn_stream_t stream) {
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
+  sa::PrepareArgs a;
+  TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
+                     rope_sin, rope_dim, S_pad, a));
+  struct {
+    const char* n;
+    const void* p;
+  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale},
+              {"k_scale", k_scale}, {"v_scale", v_scale}, {"workspace", workspace}};
+  for (auto& t : outs) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  if (workspace_bytes < workspace_needed)
+    return fail(ATTN_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu required", who, workspace_bytes,
+                workspace_needed);
+  TRY(check_device());
   a.q_i8 = q_i8;
   a.k_i8 = k_i8;
   a.v_fp8 = v_fp8;
   a.q_scale = q_scale;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
-  a.c_log2 = (float)((double)softmax_scale * kLog2e);
   a.vmax = reinterpret_cast<uint32_t*>(workspace);
   if (k_mean != nullptr) {
     a.k_mean = k_mean;
@@ -488,6 +500,99 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
   e = sa::launch_sage_attn_pv16(tq, tk, tv, q_scale, k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
                                 (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd_pv16 launch");
+  return ATTN_OK;
+}
+
+// Workspace of sage_attention: consecutive 256-byte aligned pieces.
+struct FusedLayout {
+  size_t q16, k16, q_scale, k_scale, v_fp8, v_scale, vmax, k_mean, k_partial, total;
+};
+static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16) {
+  FusedLayout L{};
+  const size_t bh = (size_t)B * (size_t)H, nblk = (size_t)(S_pad / 32);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) & ~size_t(255);
+    return at;
+  };
+  L.q16 = take(bh * (size_t)S_pad * 128 * 2);
+  L.k16 = take(bh * (size_t)S_pad * 128 * 2);
+  L.q_scale = take(bh * nblk * 4);
+  L.k_scale = take(bh * nblk * 4);
+  if (!pv_bf16) {
+    L.v_fp8 = take(bh * 128 * (size_t)S_pad);
+    L.v_scale = take(bh * 128 * 4);
+    L.vmax = take(bh * 128 * 4);
+  }
+  if (smooth_k) {
+    L.k_mean = take(bh * 128 * 4);
+    L.k_partial = take(bh * nblk * 128 * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16) {
+  if (B < 1 || H < 1 || S_pad < 1) return 0;
+  return fused_layout(B, H, S_pad, smooth_k, pv_bf16).total;
+}
+
+attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                           const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                           float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                           const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_k, int pv_bf16,
+                           void* o, const int64_t o_str[3], void* workspace, size_t workspace_bytes,
+                           attn_stream_t stream) {
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
+  if ((smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1))
+    return fail(ATTN_ERR_INVALID_ARG, "smooth_k=%d and pv_bf16=%d must be 0 or 1", smooth_k, pv_bf16);
+  const int64_t S_pad = sage_padded_len(S);
+  sa::PrepareArgs a;
+  TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
+                     rope_sin, rope_dim, S_pad, a));
+  long long os[3];
+  TRY(check_strides("o", o, o_str, B, S, H, os));
+  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
+  const FusedLayout L = fused_layout(B, H, S_pad, smooth_k, pv_bf16);
+  if (workspace_bytes < L.total)
+    return fail(ATTN_ERR_INVALID_ARG, "sage_attention: workspace_bytes=%zu < %zu required", workspace_bytes, L.total);
+  TRY(check_device());
+  TRY(get_encoder());
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  a.q16 = ws + L.q16;
+  a.k16 = ws + L.k16;
+  a.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
+  a.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
+  a.skip_v = pv_bf16 != 0;
+  if (!pv_bf16) {
+    a.v_fp8 = ws + L.v_fp8;
+    a.v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+    a.vmax = reinterpret_cast<uint32_t*>(ws + L.vmax);
+  }
+  if (smooth_k) {
+    a.k_mean = reinterpret_cast<float*>(ws + L.k_mean);
+    a.k_partial = reinterpret_cast<float*>(ws + L.k_partial);
+  }
+  cudaError_t e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attention prepare");
+  const long long bh = (long long)B * H;
+  CUtensorMap tq, tk, tv;
+  TRY(tmap_f16_rows(&tq, a.q16, S_pad, bh));
+  TRY(tmap_f16_rows(&tk, a.k16, S_pad, bh));
+  if (pv_bf16) {
+    TRY(tmap_bhsd_bf16(&tv, v, B, S, H, a.str[2]));
+    e = sa::launch_sage_attn_pv16(tq, tk, tv, a.q_scale, a.k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                  (cudaStream_t)stream);
+  } else {
+    TRY(tmap_bytes_3d(&tv, a.v_fp8, S_pad, 128, bh));
+    e = sa::launch_sage_attn(tq, tk, tv, a.q_scale, a.k_scale, a.v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                             (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "sage_attention launch");
   return ATTN_OK;
 }
 

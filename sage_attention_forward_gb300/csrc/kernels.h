@@ -42,6 +42,9 @@ struct PrepareArgs {
   uint32_t* vmax;            // workspace: B*H*128 words
   float* k_mean = nullptr;   // K smoothing: output [B*H*128] (nullptr: no smoothing)
   float* k_partial = nullptr;  // K smoothing workspace: [B*H, S_pad/32, 128] block sums
+  void* q16 = nullptr;       // when set: Q/K codes written as FP16 [B*H, S_pad, 128] here, not as INT8
+  void* k16 = nullptr;
+  bool skip_v = false;       // V not prepared (the 16-bit P V mode reads the BF16 input)
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 

@@ -21,6 +21,7 @@
 // loads 16 positions x 8 channels, encodes them and transposes the bytes in
 // registers (byte permutes) into 8 rows of 16 consecutive positions, which it
 // writes with 128-bit stores into the [B, H, 128, S_pad] layout.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -43,6 +44,7 @@ struct QKParams {
   const __nv_bfloat16* rope_sin;
   int rope_dim;
   int8_t* codes[2];
+  __half* codes16[2];               // when set: the codes as FP16 (exact), [B*H, S_pad, 128], instead of INT8
   float* scales[2];
   float c_log2;                     // fl32(softmax_scale * log2 e), folded into Q's scales
   uint32_t* vmax;                   // [B*H*128] float bits of the channel maxima of |V|
@@ -240,21 +242,40 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
   for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
   const float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
   int8_t* out = p.codes[task] + ((long long)bh * p.S_pad) * 128 + 16 * L;
+  __half* out16 = p.codes16[task] ? p.codes16[task] + ((long long)bh * p.S_pad) * 128 + 16 * L : nullptr;
 #pragma unroll
   for (int step = 0; step < 8; ++step) {
     const int s = 32 * blk + 4 * step + g;
-    uint32_t q[4] = {0u, 0u, 0u, 0u};
+    int c[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i] = 0;
     if (s < p.S) {
       float f[16];
       unpack16(x[step], f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         int v = __float2int_rn(__fmul_rn(smooth ? __fsub_rn(f[i], mu[i]) : f[i], inv));
-        v = max(-127, min(127, v));
-        q[i >> 2] |= (uint32_t)(v & 0xff) << (8 * (i & 3));
+        c[i] = max(-127, min(127, v));
       }
     }
-    *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
+    if (out16) {
+      // the same codes as FP16, exact (|code| <= 127): the operand the attention kernel's
+      // Q K^T MMA reads
+      uint32_t h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __half2 hv = __halves2half2(__int2half_rn(c[2 * i]), __int2half_rn(c[2 * i + 1]));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      uint4* d = reinterpret_cast<uint4*>(out16 + (long long)s * 128);
+      d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    } else {
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) q[i >> 2] |= (uint32_t)(c[i] & 0xff) << (8 * (i & 3));
+      *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
+    }
   }
   if (lane == 0) {
     float sc = 0.0f;
@@ -416,8 +437,11 @@ cudaError_t noalloc_prepare_scratch(uint32_t** out) {
 
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   const int nblk = (int)(a.S_pad / 32);
-  cudaError_t e = cudaMemsetAsync(a.vmax, 0, (size_t)a.B * a.H * 128 * sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.skip_v) {
+    e = cudaMemsetAsync(a.vmax, 0, (size_t)a.B * a.H * 128 * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   QKParams p;
   for (int t = 0; t < 3; ++t) {
     p.x[t] = reinterpret_cast<const __nv_bfloat16*>(a.x[t]);
@@ -438,6 +462,8 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   p.rope_dim = a.rope_dim;
   p.codes[0] = a.q_i8;
   p.codes[1] = a.k_i8;
+  p.codes16[0] = reinterpret_cast<__half*>(a.q16);
+  p.codes16[1] = reinterpret_cast<__half*>(a.k16);
   p.scales[0] = a.q_scale;
   p.scales[1] = a.k_scale;
   p.c_log2 = a.c_log2;
@@ -452,10 +478,11 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 g1((nblk + 7) / 8, a.B * a.H, 3);
+  dim3 g1((nblk + 7) / 8, a.B * a.H, a.skip_v ? 2 : 3);   // grid.z = 2: Q and K only
   prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (a.skip_v) return cudaSuccess;
 
   VParams vp;
   vp.v = reinterpret_cast<const __nv_bfloat16*>(a.x[2]);
