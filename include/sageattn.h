@@ -24,6 +24,15 @@
  *                   request, commit message of gfx1201_sage_attention:
  *                   "gfx1201_sage_attention_fwd runs the kernel alone on
  *                   prepared tensors".)
+ *   sage_attention  prepare + kernel as one call (that pull request's
+ *                   gfx1201_sage_attention op), the prepared tensors kept in
+ *                   the caller's workspace.
+ *
+ * Beyond those: sage_prepare_smooth_k (K smoothing before the INT8
+ * quantisation) and sage_attn_fwd_pv16 (P V in 16 bits with V unquantised),
+ * both from the handbook's SageAttention section; sage_prepare_noalloc (no
+ * workspace argument); attn_selftest_wait_timeout (exercises the failure path);
+ * sizes and status helpers.
  *
  * Conventions shared by every call
  *   - D (head dimension) must be 128; S >= 1 (attention over no keys is undefined:
@@ -39,8 +48,10 @@
  *     [B, H, S, D] storage seen through its [B, S, H, D] permutation are
  *     accepted as they are.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
- *     default stream) and enqueue kernels only.  Argument errors are found on
- *     the host before anything is enqueued.
+ *     default stream) and enqueue kernels and memsets only (except
+ *     attn_get_device_status and attn_selftest_wait_timeout, which
+ *     synchronise).  Argument errors are found on the host before anything is
+ *     enqueued.
  *   - Each call returns ATTN_OK or an error; attn_last_error() gives the
  *     message of the calling thread's last failed call.
  *   - Device-side pipeline waits are bounded (about 2 s).  A wait that runs
