@@ -384,8 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
-      const float4 ks4 = ks_next;
-      if (kInt8 && j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
+      // K scales of the tile's four 32-key blocks: prefetched a tile ahead in the FP8 mode;
+      // the 16-bit mode, whose BF16 P takes twice the registers, loads them when needed
+      float4 ks4 = ks_next;
+      if constexpr (kFP8) {
+        if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
+      } else if constexpr (kInt8) {
+        ks4 = __ldg(reinterpret_cast<const float4*>(ksp + 4 * j));
+      }
       const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
       if (!mbar_wait_warp<false>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
       tc_fence_after();

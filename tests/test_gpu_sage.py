@@ -20,7 +20,8 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from parity import (SAGE_A, SAGE_B, assert_sage_exact_gate, assert_sage_format_gate, gather_rows, metrics)
+from parity import (BF16_A, BF16_B, SAGE_A, SAGE_B, assert_sage_exact_gate, assert_sage_format_gate,
+                    gather_rows, metrics)
 from workloads import make_inputs, sample_rows, small_case, to_device
 
 pytestmark = pytest.mark.gpu
@@ -143,3 +144,47 @@ def test_permuted_output_layout_both_modes(cuda_dev, workload_inputs):
         assert torch.equal(o_perm, o_contig)
         del o_contig, o_store, o_perm
     sa.attn_get_device_status()
+
+
+@pytest.mark.parametrize("pv", ["e4m3", "bf16"])
+def test_key_value_reversal_permutes_the_format(cuda_dev, pv):
+    """Reversing the K/V tokens (the aiter pull request, Test Result: the
+    K/V-reversal noise floor) with S a multiple of 32.  Reversal maps whole
+    32-row K blocks onto blocks and leaves V's per-channel maxima unchanged, so
+    the prepared K and V are exactly the forward order's codes and scales,
+    permuted.  The exact value of the format is therefore the same.  The output
+    may move only by the kernel's rounding, which depends on the key order
+    (summation order and, in the e4m3 mode, the running maximum P is scaled by):
+    both orders pass the format and exact gates."""
+    S, H = 544, 2                   # 17 blocks of 32 keys; padded to 640
+    inp = make_inputs(small_case(1, H, S, 17))
+    g = to_device(inp, cuda_dev)
+    rev = torch.arange(S - 1, -1, -1, device=cuda_dev)
+    k_r, v_r = g.k[:, rev].contiguous(), g.v[:, rev].contiguous()
+    p1 = sa.sage_prepare(g.q, g.k, g.v)
+    p2 = sa.sage_prepare(g.q, k_r, v_r)
+    torch.cuda.synchronize()
+    assert torch.equal(p2.q_i8, p1.q_i8) and torch.equal(p2.q_scale, p1.q_scale)
+    nb = S // 32
+    assert torch.equal(p2.k_i8[:, :, :S], p1.k_i8[:, :, rev])
+    assert torch.equal(p2.k_scale[..., :nb], p1.k_scale[..., :nb].flip(-1))
+    assert torch.equal(p2.v_fp8[..., :S], p1.v_fp8[..., rev])
+    assert torch.equal(p2.v_scale, p1.v_scale)
+    if pv == "e4m3":
+        o1, o2 = sa.sage_attn_fwd(p1), sa.sage_attn_fwd(p2)
+    else:
+        o1, o2 = sa.sage_attn_fwd_pv16(p1, g.v), sa.sage_attn_fwd_pv16(p2, v_r)
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    rows = oracle.all_rows(1, S, H)
+    prep = oracle.prepare(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
+    if pv == "e4m3":
+        check(o1, inp, rows, "forward order")
+        check(o2, inp, rows, "reversed order")
+        a_abs_v, a, b = oracle.sage_attention(prep, S, rows, H, abs_v=True), SAGE_A, SAGE_B
+    else:
+        a_abs_v, a, b = oracle.sage_attention_v16(prep, inp.v, rows, abs_v=True), BF16_A, BF16_B
+    # each order lies within a + b A|V| of the same exact value, so the two within twice that
+    d = metrics(gather_rows(o2, rows), gather_rows(o1, rows), a_abs_v, 2 * a, 2 * b)
+    print(pv, "reversed vs forward:", d)
+    assert d["bound_ratio"] <= 1.0 and d["cos"] >= 0.999, d

@@ -70,3 +70,27 @@ def test_rounded_p_reproduces_the_printed_accuracy_band():
     # without the rounding of P the format alone is clearly more accurate
     exact = oracle.sage_attention(prep, 2048, rows, 4)
     assert np.linalg.norm(exact - ref) / np.linalg.norm(ref) < 0.8 * rel
+
+
+def test_key_value_reversal_permutes_codes_and_keeps_the_format_value():
+    """With S a multiple of 32, reversing the K/V tokens maps whole K blocks
+    onto blocks and keeps V's per-channel maxima, so the oracle's codes are the
+    forward order's, permuted, and the FP64 attention of the format is the same
+    up to summation order.  A wrong block index, or V's transpose taken on the
+    wrong axis, breaks the permutation."""
+    S, H = 192, 2
+    inp = make_inputs(small_case(1, H, S, 57))
+    sm = 1 / math.sqrt(128)
+    rev = torch.arange(S - 1, -1, -1)
+    a = oracle.prepare(inp.q, inp.k, inp.v, sm)
+    b = oracle.prepare(inp.q, inp.k[:, rev], inp.v[:, rev], sm)
+    assert torch.equal(b["q_i8"], a["q_i8"]) and torch.equal(b["q_scale"], a["q_scale"])
+    nb = S // 32
+    assert torch.equal(b["k_i8"][:, :, :S], a["k_i8"][:, :, rev])
+    assert torch.equal(b["k_scale"][..., :nb], a["k_scale"][..., :nb].flip(-1))
+    assert torch.equal(b["v_fp8"][..., :S], a["v_fp8"][..., rev])
+    assert torch.equal(b["v_scale"], a["v_scale"])
+    rows = oracle.all_rows(1, S, H)
+    oa = oracle.sage_attention(a, S, rows, H)
+    ob = oracle.sage_attention(b, S, rows, H)
+    assert np.abs(oa - ob).max() <= 1e-12
