@@ -7,6 +7,19 @@
 // inputs, and the order of the one order-dependent sum (RMSNorm's sum of
 // squares) is fixed below.
 //
+// Instruction selection keeps the instruction count low while every result
+// stays that of the rounded operation it implements: BF16 roundings of binary32
+// values go in pairs (cvt.rn.bf16x2.f32, which also packs the pair for the next
+// stage); a BF16 x BF16 product or BF16 + BF16 sum that eager arithmetic rounds
+// from binary32 is one mul/add.rn.bf16x2 (the same value, see bf2_mul); the RoPE
+// term -partner*sin is the rounded partner*sin with its sign bits flipped
+// (rounding to nearest even is sign-symmetric); block maxima of |BF16| values
+// are taken on the packed pairs (max.bf16x2); and the INT8 code
+// clamp(rne(v * inv), -127, 127) is formed as v * inv + 1.5 * 2^23, whose
+// addition rounds to the integer and leaves it in the low mantissa bits.
+// (NaN, which only RMSNorm of an all-zero or underflowing row with rms_eps = 0
+// produces, has no defined code.)
+//
 // Kernel 1 (grid.z = 0: Q, 1: K, 2: V maxima) -- one warp per (b, h, 32-row
 // block).  A row of 128 channels is held by 8 lanes, lane L of the group owning
 // channels [16L, 16L + 16) (two 128-bit loads); a warp covers 4 rows per step
@@ -25,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -53,14 +67,6 @@ struct QKParams {
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-__device__ __forceinline__ float bf_round(float f) {
-  return __bfloat162float(__float2bfloat16_rn(f));
-}
-__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
-  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return l | (h << 16);
-}
 __device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&f)[16]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -68,10 +74,38 @@ __device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&f)[16])
     f[2 * i + 1] = bf_hi(w[i]);
   }
 }
-__device__ __forceinline__ void pack16(const float (&f)[16], uint32_t (&w)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = bf_pack(f[2 * i], f[2 * i + 1]);
+// Two floats rounded to BF16 (nearest even) by one paired conversion; the result
+// holds lo in its low half, as the [.., 128] rows store channel pairs.
+__device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
+// Products and sums of two BF16 values, rounded once to BF16 (mul/add.rn.bf16x2).
+// Eager BF16 arithmetic computes them in binary32 and rounds that to BF16; the two
+// agree for all finite operands.  A product of two 8-bit significands is exact in
+// binary32 down to 2^-149, and below that it lies under the smallest BF16 rounding
+// midpoint (2^-134) either way.  A sum is exact in binary32 unless the exponents
+// differ by more than 15, and then the smaller term is far below half a BF16 ulp
+// of the larger, so both roundings return the larger.
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Per-half maximum of two BF16 pairs (max.bf16x2).
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// 1.5 * 2^23: for |v| < 2^22, v + kRoundMagic is rounded to an integer (nearest even) by the
+// addition itself, and that integer n is stored in the low mantissa bits: bits = 0x4B400000 + n.
+constexpr float kRoundMagic = 12582912.0f;
 __device__ __forceinline__ void load16(const __nv_bfloat16* src, uint32_t (&w)[8]) {
   const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
   const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
@@ -107,8 +141,6 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
   if (nw != nullptr) {
     uint32_t ww[8];
     load16(nw + 16 * L, ww);
-    float wf[16];
-    unpack16(ww, wf);
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
       float f[16];
@@ -119,11 +151,11 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-      const float ms = __fmul_rn(acc, 1.0f / 128.0f);
-      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(acc, 1.0f / 128.0f), p.eps)));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) f[i] = bf_round(__fmul_rn(bf_round(__fmul_rn(f[i], r)), wf[i]));
-      pack16(f, x[step]);
+      for (int i = 0; i < 8; ++i) {
+        x[step][i] = bf2_mul(bf2_bits(__fmul_rn(f[2 * i], r), __fmul_rn(f[2 * i + 1], r)), ww[i]);
+      }
     }
   }
 
@@ -135,6 +167,7 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
     int src = lo_half ? L + (hh >> 4) : L - (hh >> 4);
     if (!in_rope) src = L;
     const int src_lane = (lane & ~7) | src;
+    const uint32_t neg = lo_half ? 0x80008000u : 0u;
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
       uint32_t partner[8];
@@ -145,19 +178,11 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
         uint32_t cw[8], sw[8];
         load16(p.rope_cos + (long long)s * p.rope_dim + 16 * L, cw);
         load16(p.rope_sin + (long long)s * p.rope_dim + 16 * L, sw);
-        float f[16], pf[16], cf[16], sf[16];
-        unpack16(x[step], f);
-        unpack16(partner, pf);
-        unpack16(cw, cf);
-        unpack16(sw, sf);
+        // x*cos + rot*sin with rot = -partner on the low half: round(-u) = -round(u) under
+        // nearest-even rounding, so the rounded partner*sin pair has its signs flipped instead
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float rot = lo_half ? -pf[i] : pf[i];
-          const float a = bf_round(__fmul_rn(f[i], cf[i]));
-          const float bb = bf_round(__fmul_rn(rot, sf[i]));
-          f[i] = bf_round(__fadd_rn(a, bb));
-        }
-        pack16(f, x[step]);
+        for (int i = 0; i < 8; ++i)
+          x[step][i] = bf2_add(bf2_mul(x[step][i], cw[i]), bf2_mul(partner[i], sw[i]) ^ neg);
       }
     }
   }
@@ -178,9 +203,9 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
   if (task == 2) {
     // -------------------------------------------------------- V channel maxima
     __shared__ float red[8][128];
-    float mx[16];
+    uint32_t m2[8];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) mx[k] = 0.0f;
+    for (int i = 0; i < 8; ++i) m2[i] = 0u;
     if (blk < p.nblk) {
 #pragma unroll
       for (int step = 0; step < 8; ++step) {
@@ -188,13 +213,13 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
         if (s < p.S) {
           uint32_t w[8];
           load16(base + (long long)s * ss, w);
-          float f[16];
-          unpack16(w, f);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) mx[k] = fmaxf(mx[k], fabsf(f[k]));
+          for (int i = 0; i < 8; ++i) m2[i] = bf2_max(m2[i], w[i] & 0x7fff7fffu);
         }
       }
     }
+    float mx[16];
+    unpack16(m2, mx);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], 8));
@@ -228,55 +253,76 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
 
   // ---------------------------------------------------------- block maximum and INT8 codes
   float a = 0.0f;
+  if (smooth) {
 #pragma unroll
-  for (int step = 0; step < 8; ++step) {
-    const int s = 32 * blk + 4 * step + g;
-    if (s < p.S) {
-      float f[16];
-      unpack16(x[step], f);
+    for (int step = 0; step < 8; ++step) {
+      const int s = 32 * blk + 4 * step + g;
+      if (s < p.S) {
+        float f[16];
+        unpack16(x[step], f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(smooth ? __fsub_rn(f[i], mu[i]) : f[i]));
+        for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(__fsub_rn(f[i], mu[i])));
+      }
     }
+  } else {
+    // |x| of BF16 values is exact, so the maximum is taken on the BF16 pairs (rows >= S are 0)
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int step = 0; step < 8; ++step)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m2 = bf2_max(m2, x[step][i] & 0x7fff7fffu);
+    a = fmaxf(bf_lo(m2), bf_hi(m2));
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
   const float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
   int8_t* out = p.codes[task] + ((long long)bh * p.S_pad) * 128 + 16 * L;
   __half* out16 = p.codes16[task] ? p.codes16[task] + ((long long)bh * p.S_pad) * 128 + 16 * L : nullptr;
+  // code = clamp(round_nearest_even(v * inv), -127, 127), the rounding done by adding
+  // kRoundMagic to v * inv clamped to [-127, 127] (the same integer).  With a finite inv the
+  // clamp never binds: |v| <= a, so |v * inv| <= 127 (1 + 2^-24) before rounding, which rounds
+  // to 127.  Only when 127 / a overflows (a whole block below 3.7e-37) is it needed; the
+  // block is one warp's, so the choice is warp-uniform.  Rows >= S code to 0.
+  auto emit_codes = [&](auto kClamp) {
 #pragma unroll
-  for (int step = 0; step < 8; ++step) {
-    const int s = 32 * blk + 4 * step + g;
-    int c[16];
+    for (int step = 0; step < 8; ++step) {
+      const int s = 32 * blk + 4 * step + g;
+      const bool live = s < p.S;
+      auto code = [&](float f, int i) {
+        float v = __fmul_rn(smooth ? __fsub_rn(f, mu[i]) : f, inv);
+        if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
+        return live ? __fadd_rn(v, kRoundMagic) : kRoundMagic;
+      };
+      if (out16) {
+        // the same codes as FP16, exact (|code| <= 127): the operand the attention kernel's
+        // Q K^T MMA reads
+        uint32_t hw[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) c[i] = 0;
-    if (s < p.S) {
-      float f[16];
-      unpack16(x[step], f);
+        for (int i = 0; i < 8; ++i) {
+          const float y0 = code(bf_lo(x[step][i]), 2 * i), y1 = code(bf_hi(x[step][i]), 2 * i + 1);
+          const __half2 hv = __floats2half2_rn(__fsub_rn(y0, kRoundMagic), __fsub_rn(y1, kRoundMagic));
+          hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        uint4* d = reinterpret_cast<uint4*>(out16 + (long long)s * 128);
+        d[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        d[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+      } else {
+        // the code's two's-complement byte is the low byte of its kRoundMagic sum
+        uint32_t q[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        int v = __float2int_rn(__fmul_rn(smooth ? __fsub_rn(f[i], mu[i]) : f[i], inv));
-        c[i] = max(-127, min(127, v));
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t lo = __byte_perm(__float_as_uint(code(bf_lo(x[step][2 * w]), 4 * w)),
+                                          __float_as_uint(code(bf_hi(x[step][2 * w]), 4 * w + 1)), 0x0040);
+          const uint32_t hi = __byte_perm(__float_as_uint(code(bf_lo(x[step][2 * w + 1]), 4 * w + 2)),
+                                          __float_as_uint(code(bf_hi(x[step][2 * w + 1]), 4 * w + 3)), 0x0040);
+          q[w] = __byte_perm(lo, hi, 0x5410);
+        }
+        *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
       }
     }
-    if (out16) {
-      // the same codes as FP16, exact (|code| <= 127): the operand the attention kernel's
-      // Q K^T MMA reads
-      uint32_t h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const __half2 hv = __halves2half2(__int2half_rn(c[2 * i]), __int2half_rn(c[2 * i + 1]));
-        h[i] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      uint4* d = reinterpret_cast<uint4*>(out16 + (long long)s * 128);
-      d[0] = make_uint4(h[0], h[1], h[2], h[3]);
-      d[1] = make_uint4(h[4], h[5], h[6], h[7]);
-    } else {
-      uint32_t q[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 16; ++i) q[i >> 2] |= (uint32_t)(c[i] & 0xff) << (8 * (i & 3));
-      *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
-    }
-  }
+  };
+  if (isinf(inv)) emit_codes(std::true_type{});
+  else emit_codes(std::false_type{});
   if (lane == 0) {
     float sc = 0.0f;
     if (a > 0.0f) {

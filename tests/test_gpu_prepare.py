@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from workloads import make_inputs, rope_tables, small_case, to_device
+from workloads import make_inputs, rope_tables, small_case, to_device, wide_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,37 @@ def test_fused_equals_unfused(cuda_dev):
     torch.cuda.synchronize()
     for name in ("q_i8", "k_i8", "v_fp8", "q_scale", "k_scale", "v_scale"):
         assert torch.equal(getattr(prep, name), getattr(plain, name)), name
+
+
+def test_extreme_magnitudes_bit_exact(cuda_dev):
+    """Q/K blocks at the ends of the BF16 range: blocks whose largest |x| is so
+    small that 127 / max overflows to infinity (every code is then +-127),
+    subnormal blocks, blocks near the BF16 maximum and blocks spanning 2^-120 to
+    2^120; V of magnitudes 2^-100 to 2^100.  Bit-exact against the oracle."""
+    S, H = 256, 2
+    ranges = [(-130, -123), (-120, 120), (100, 127), (-133, -126), (-20, 20), (-126, -100), (0, 1), (-60, 60)]
+    def qk(seed):
+        return torch.cat([wide_bf16(seed + i, (1, 32, H, 128), lo, hi) for i, (lo, hi) in enumerate(ranges)], dim=1)
+    inp = make_inputs(small_case(1, H, S, 61))
+    inp.q, inp.k, inp.v = qk(100), qk(200), wide_bf16(300, (1, S, H, 128), -100, 100)
+    prep, exp = run(inp, cuda_dev)
+    assert_prepared_equal(prep, exp, "extreme magnitudes")
+    codes = prep.q_i8[0, 0, :32].cpu()
+    assert (codes.abs() == 127).all()                     # the overflowing block
+
+
+def test_norm_rope_extreme_tables_bit_exact(cuda_dev):
+    """RMSNorm weights of magnitude 2^-100 to 2^20 (Q) and 2^-125 to 2^-95 (K),
+    RoPE tables of 2^-60 to 2^10 (any BF16 tables are valid input): K's rounded
+    products reach the BF16 subnormal range and below (7 % of its values end
+    subnormal, 15 % zero), where eager BF16 rounds the binary32 result and the
+    prepare rounds a BF16 product directly.  Bit-exact against the oracle."""
+    S, H, rd = 256, 2, 64
+    inp = make_inputs(small_case(1, H, S, 62, rms_norm=True, rope_dim=rd))
+    inp.q_norm_w, inp.k_norm_w = wide_bf16(400, (128,), -100, 20), wide_bf16(401, (128,), -125, -95)
+    inp.rope_cos, inp.rope_sin = wide_bf16(402, (S, rd), -60, 10), wide_bf16(403, (S, rd), -60, 10)
+    prep, exp = run(inp, cuda_dev)
+    assert_prepared_equal(prep, exp, "extreme norm weights and RoPE tables")
 
 
 @pytest.mark.parametrize("name", ["tiny", "flux1024", "flux2048", "wan720p", "hunyuan720p"])

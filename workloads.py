@@ -173,6 +173,17 @@ def make_inputs(wl: Workload, device="cpu") -> Inputs:
     return inp
 
 
+def wide_bf16(seed: int, shape, lo_exp: int, hi_exp: int) -> torch.Tensor:
+    """BF16 values of random sign with magnitudes m * 2^e, m ~ U[1, 2) and the
+    integer e ~ U[lo_exp, hi_exp): inputs at the ends of the BF16 range
+    (subnormals from e = -133, near the maximum up to e = 127)."""
+    g = _gen(seed, "cpu")
+    e = torch.randint(lo_exp, hi_exp, shape, generator=g).to(torch.float64)
+    m = 1.0 + torch.rand(shape, generator=g, dtype=torch.float64)
+    sign = torch.where(torch.rand(shape, generator=g) < 0.5, -1.0, 1.0).to(torch.float64)
+    return (sign * m * torch.pow(2.0, e)).to(torch.bfloat16)
+
+
 def to_device(inp: Inputs, device) -> Inputs:
     """Copy every tensor to `device`, keeping the logical strides of q/k/v."""
     def mv(t):
