@@ -628,7 +628,8 @@ attn_status attn_get_device_status(attn_stream_t stream) {
   if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
   if (w)
     return fail(ATTN_ERR_DEVICE_TIMEOUT,
-                "an attention kernel gave up on a bounded wait (bits 0x%x: 1 TMA load, 2 MMA commit, 4 hand-off)", w);
+                "an attention kernel gave up on a bounded wait (bits 0x%x: 1 TMA load, 2 MMA commit, 4 hand-off; "
+                "0x100 a check build's TMEM-maximum mismatch)", w);
   return ATTN_OK;
 }
 

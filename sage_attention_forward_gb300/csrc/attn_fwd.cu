@@ -401,28 +401,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t(&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
       uint32_t(&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
       const int valid = p.S - j * kBN;
-      float m_cand;
-      tmem_ld32(tS + 0, s0);
-      tmem_ld32(tS + 32, s1);
+      float m_cand, r0, r1, r2, r3;
+      // the loads also return each 32-key block's largest raw score
+      tmem_ld32_max(tS + 0, s0, r0);
+      tmem_ld32_max(tS + 32, s1, r1);
       tmem_ld_wait();
       tmem_reg_fence(s0);
       tmem_reg_fence(s1);
-      tmem_ld32(tS + 64, s2);
-      tmem_ld32(tS + 96, s3);
+      tmem_reg_fence2f(r0, r1);
+      tmem_ld32_max(tS + 64, s2, r2);
+      tmem_ld32_max(tS + 96, s3, r3);
       // scales are >= 0, so a key block's largest t is f * (largest raw score); a block
       // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
       if (valid >= kBN) {
-        // the first half's maximum overlaps the second half's load
-        const float m01 = fmaxf(max32(&s[0]) * f[0], max32(&s[32]) * f[1]);
+        const float m01 = fmaxf(r0 * f[0], r1 * f[1]);
         tmem_ld_wait();
         tmem_reg_fence(s2);
         tmem_reg_fence(s3);
-        m_cand = fmaxf(m01, fmaxf(max32(&s[64]) * f[2], max32(&s[96]) * f[3]));
+        tmem_reg_fence2f(r2, r3);
+        m_cand = fmaxf(m01, fmaxf(r2 * f[2], r3 * f[3]));
+#ifdef SAGEATTN_CHECK_TMEM_MAX
+        // check build: the same maximum formed from the loaded scores themselves
+        const float m_sw = fmaxf(fmaxf(max32(&s[0]) * f[0], max32(&s[32]) * f[1]),
+                                 fmaxf(max32(&s[64]) * f[2], max32(&s[96]) * f[3]));
+        if (!(m_sw == m_cand)) atomicOr(&g_err_attn, kErrCheckTmemMax);
+        m_cand = m_sw;
+#endif
       } else {
         // keys past S: excluded from the maximum here and given probability 0 below
         tmem_ld_wait();
         tmem_reg_fence(s2);
         tmem_reg_fence(s3);
+        tmem_reg_fence2f(r2, r3);
 #pragma unroll
         for (int e = 0; e < 128; ++e)
           if (e >= valid) s[e] = f2u(-INFINITY);

@@ -16,6 +16,7 @@ enum : uint32_t {
   kErrTimeoutTma = 1u << 0,   // a TMA transfer never completed
   kErrTimeoutMma = 1u << 1,   // an MMA commit never arrived
   kErrTimeoutSync = 1u << 2,  // a producer/consumer hand-off never arrived
+  kErrCheckTmemMax = 1u << 8, // check builds only: a tcgen05.ld.red maximum disagreed with the loaded values
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer time.
@@ -174,6 +175,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// The same load, also returning the largest of the 32 loaded values (sm_103a
+// tcgen05.ld.red; NaN inputs are ignored as by max.f32).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& m) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=f"(m)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_reg_fence2f(float& a, float& b) { asm volatile("" : "+f"(a), "+f"(b)); }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "

@@ -141,21 +141,43 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
   if (nw != nullptr) {
     uint32_t ww[8];
     load16(nw + 16 * L, ww);
+    // the sum of squares of each row (the same order in every lane of the row's group);
+    // lane L of a group keeps the sum of its step-L row, takes 1 / sqrt(mean + eps) of it
+    // once, and the group's lanes fetch each step's factor from lane L = step by a shuffle
+    float mine = 0.0f;
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
-      float f[16];
-      unpack16(x[step], f);
       float acc = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc = __fadd_rn(acc, __fmul_rn(f[i], f[i]));
+      for (int i = 0; i < 8; ++i) {
+        // unpacked by byte permutes, not the shifts the scaling below uses, so that the
+        // compiler recomputes them there instead of holding 128 floats across the shuffles
+        const float lo = __uint_as_float(__byte_perm(x[step][i], 0u, 0x1044));
+        const float hi = __uint_as_float(__byte_perm(x[step][i], 0u, 0x3244));
+        acc = __fadd_rn(acc, __fmul_rn(lo, lo));
+        acc = __fadd_rn(acc, __fmul_rn(hi, hi));
+      }
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-      const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(acc, 1.0f / 128.0f), p.eps)));
+      mine = (L == step) ? acc : mine;
+    }
+    const float r_mine = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(mine, 1.0f / 128.0f), p.eps)));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[step][i] = bf2_mul(bf2_bits(__fmul_rn(f[2 * i], r), __fmul_rn(f[2 * i + 1], r)), ww[i]);
-      }
+    for (int step = 0; step < 8; ++step) {
+      const float r = __shfl_sync(0xffffffffu, r_mine, (lane & ~7) | step);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[step][i] = bf2_mul(bf2_bits(__fmul_rn(bf_lo(x[step][i]), r), __fmul_rn(bf_hi(x[step][i]), r)), ww[i]);
+    }
+    // rows >= S stay exact zeros (with rms_eps = 0 their factor is infinite); only the last
+    // block has such rows
+    if (32 * blk + 32 > p.S) {
+#pragma unroll
+      for (int step = 0; step < 8; ++step)
+        if (32 * blk + 4 * step + g >= p.S)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[step][i] = 0u;
     }
   }
 
@@ -283,15 +305,22 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
   // clamp never binds: |v| <= a, so |v * inv| <= 127 (1 + 2^-24) before rounding, which rounds
   // to 127.  Only when 127 / a overflows (a whole block below 3.7e-37) is it needed; the
   // block is one warp's, so the choice is warp-uniform.  Rows >= S code to 0.
-  auto emit_codes = [&](auto kClamp) {
+  auto emit_codes = [&](auto kClamp, auto kSmooth) {
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
       const int s = 32 * blk + 4 * step + g;
       const bool live = s < p.S;
       auto code = [&](float f, int i) {
-        float v = __fmul_rn(smooth ? __fsub_rn(f, mu[i]) : f, inv);
-        if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
-        return live ? __fadd_rn(v, kRoundMagic) : kRoundMagic;
+        if constexpr (decltype(kSmooth)::value) {
+          float v = __fmul_rn(__fsub_rn(f, mu[i]), inv);
+          if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
+          return live ? __fadd_rn(v, kRoundMagic) : kRoundMagic;
+        } else {
+          // rows >= S hold zeros here, which code to 0
+          float v = __fmul_rn(f, inv);
+          if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
+          return __fadd_rn(v, kRoundMagic);
+        }
       };
       if (out16) {
         // the same codes as FP16, exact (|code| <= 127): the operand the attention kernel's
@@ -321,8 +350,13 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
       }
     }
   };
-  if (isinf(inv)) emit_codes(std::true_type{});
-  else emit_codes(std::false_type{});
+  if (smooth) {
+    if (isinf(inv)) emit_codes(std::true_type{}, std::true_type{});
+    else emit_codes(std::false_type{}, std::true_type{});
+  } else {
+    if (isinf(inv)) emit_codes(std::true_type{}, std::false_type{});
+    else emit_codes(std::false_type{}, std::false_type{});
+  }
   if (lane == 0) {
     float sc = 0.0f;
     if (a > 0.0f) {

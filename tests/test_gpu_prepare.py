@@ -1,6 +1,7 @@
 """sage_prepare (CUDA, through the C ABI) is bit-exact against the oracle:
 INT8 Q/K codes, e4m3 V codes and all FP32 scales, on every workload and on
 small ragged shapes, with and without the fused RMSNorm + RoPE."""
+import dataclasses
 import math
 
 import numpy as np
@@ -67,6 +68,16 @@ def test_norm_rope_bit_exact(cuda_dev, rope_dim, norm):
     inp = make_inputs(small_case(2, 3, 300, 300 + rope_dim, rms_norm=norm, rope_dim=rope_dim))
     prep, exp = run(inp, cuda_dev)
     assert_prepared_equal(prep, exp, f"norm={norm} rope_dim={rope_dim}")
+
+
+def test_norm_with_zero_eps_and_ragged_tail(cuda_dev):
+    """rms_eps = 0 (a valid argument): the padding rows of the last 32-row block,
+    zeros whose RMSNorm factor would be infinite, still code to 0 and leave the
+    block's maximum alone; the S real rows are bit-exact against the oracle."""
+    inp = make_inputs(dataclasses.replace(small_case(1, 2, 300, 63, rms_norm=True, rope_dim=64), rms_eps=0.0))
+    prep, exp = run(inp, cuda_dev)
+    assert_prepared_equal(prep, exp, "rms_eps 0, S 300")
+    assert (prep.q_i8[:, :, 300:] == 0).all() and (prep.k_i8[:, :, 300:] == 0).all()
 
 
 def test_fused_equals_unfused(cuda_dev):
