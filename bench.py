@@ -231,6 +231,7 @@ def run_ours(args, rank, world):
     prep_s = sa.Prepared.empty(B, H, S, S_pad, dev)
     ws_s = sa.prepare_workspace(B, H, dev, S_pad, smooth_k=True)
     ws_16 = sa.sage_attention_workspace(B, H, S, dev, pv="bf16")
+    ws_ql = sa.sage_attention_workspace(B, H, S, dev, q_on_load=True)
     sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw)
     calls = {
         "bf16": lambda: sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale),
@@ -240,6 +241,8 @@ def run_ours(args, rank, world):
                                    sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a)),
         "sage_pv16": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_pv16, workspace=ws_16, pv="bf16",
                                                **kw),
+        "sage_q_on_load": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_pv16, workspace=ws_ql,
+                                                    q_on_load=True, **kw),
         "sage_core": lambda: sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a),
         "sage_pv16_core": lambda: sa.sage_attn_fwd_pv16(prep, v, out=o_pv16, workspace=ws_a),
         "prepare": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p,
@@ -276,6 +279,8 @@ def run_ours(args, rank, world):
         "sage_two_calls": {"ms": ms["sage_two_calls"], "tflops": tf("sage_two_calls"),
                            "call": "sage_prepare, then sage_attn_fwd"},
         "sage_pv16": {"ms": ms["sage_pv16"], "tflops": tf("sage_pv16"), "call": "sage_attention(pv=bf16)"},
+        "sage_q_on_load": {"ms": ms["sage_q_on_load"], "tflops": tf("sage_q_on_load"),
+                           "call": "sage_attention(q_on_load=True): Q coded by the forward"},
         "sage_core": {"ms": ms["sage_core"], "tflops": tf("sage_core"),
                       # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
                       "frac_of_tensor_roof": tf("sage_core") / (peaks["bf16_sustained"] / 0.75)},
@@ -289,7 +294,7 @@ def run_ours(args, rank, world):
         "timing": "each provider alone: 2 warm-up + 5 calls, 3 interleaved rounds, median",
         "in_step_ms": step_ms,
     }
-    del prep_s, ws_s, o_pv16, ws_16
+    del prep_s, ws_s, o_pv16, ws_16, ws_ql
 
     # ------------------------------------------------------------- end to end
     e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)

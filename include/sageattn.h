@@ -271,9 +271,11 @@ ATTN_API attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, 
 
 /*
  * sage_attention_workspace_size -- bytes of device scratch sage_attention needs
- * (0 for an empty problem).  smooth_k and pv_bf16 as given to sage_attention.
+ * (0 for an empty problem).  smooth_k, pv_bf16 and q_on_load as given to
+ * sage_attention.
  */
-ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16);
+ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16,
+                                              int q_on_load);
 
 /*
  * sage_attention -- the SageAttention-style forward as one call: the prepare
@@ -282,25 +284,32 @@ ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int s
  * prepare + kernel).  The prepared tensors never leave `workspace`: the Q/K codes
  * are written there as FP16 (the exact values of the INT8 codes, the operand the
  * Q K^T MMA reads), which spares the INT8 round trip and the widening pass of
- * sage_prepare + sage_attn_fwd; the output is bit-identical to that two-call
- * sequence.
+ * sage_prepare + sage_attn_fwd.  With q_on_load = 1, Q is instead quantised
+ * inside the attention kernel as it is loaded (each row after its optional
+ * RMSNorm and RoPE, the same arithmetic as sage_prepare), so Q's codes never
+ * reach memory; on a GB300 that measured slower (the coding sits on every CTA's
+ * path to its first product, while the prepare's Q pass overlaps its K and V
+ * passes), so it is not the default.  Either way the output is bit-identical to
+ * the two-call sequence.
  *   q, k, v, strides, softmax_scale, RMSNorm and RoPE arguments : as sage_prepare
  *   smooth_k   : 0 or 1 -- K smoothing as sage_prepare_smooth_k
  *   pv_bf16    : 0 -- P and V in e4m3 (sage_attn_fwd); 1 -- P in BF16 times the
  *                BF16 V input (sage_attn_fwd_pv16; V is then not quantised)
+ *   q_on_load  : 0 -- Q coded by the prepare; 1 -- Q coded by the forward as it
+ *                is loaded
  *   o, o_str   : BF16 [B, S, H, 128] output, element strides (as sage_attn_fwd)
  *   workspace  : at least sage_attention_workspace_size(B, H, sage_padded_len(S),
- *                smooth_k, pv_bf16) bytes, 16-byte aligned; contents on entry do
- *                not matter.
- * Enqueues the prepare kernels (two to four) and the attention kernel on
- * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_k or pv_bf16
- * other than 0/1 -> ATTN_ERR_INVALID_ARG.
+ *                smooth_k, pv_bf16, q_on_load) bytes, 16-byte aligned; contents
+ *                on entry do not matter.
+ * Enqueues the prepare kernels (one to four) and the attention kernel on
+ * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_k, pv_bf16 or
+ * q_on_load other than 0/1 -> ATTN_ERR_INVALID_ARG.
  */
 ATTN_API attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                                     const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                                     float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
                                     const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_k,
-                                    int pv_bf16, void* o, const int64_t o_str[3], void* workspace,
+                                    int pv_bf16, int q_on_load, void* o, const int64_t o_str[3], void* workspace,
                                     size_t workspace_bytes, attn_stream_t stream);
 
 /*

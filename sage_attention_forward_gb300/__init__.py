@@ -80,10 +80,10 @@ def lib() -> ctypes.CDLL:
         L.sage_attn_fwd_pv16.argtypes = [_vp, _vp, _vp, _vp, _vp, _I64x3, _vp, _I64x3, i, i, i, i, ctypes.c_int64,
                                          _vp, ctypes.c_size_t, _vp]
         L.sage_attn_fwd_pv16.restype = i
-        L.sage_attention_workspace_size.argtypes = [i, i, ctypes.c_int64, i, i]
+        L.sage_attention_workspace_size.argtypes = [i, i, ctypes.c_int64, i, i, i]
         L.sage_attention_workspace_size.restype = ctypes.c_size_t
         L.sage_attention.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp, _vp,
-                                     ctypes.c_float, _vp, _vp, i, i, i, _vp, _I64x3, _vp, ctypes.c_size_t, _vp]
+                                     ctypes.c_float, _vp, _vp, i, i, i, i, _vp, _I64x3, _vp, ctypes.c_size_t, _vp]
         L.sage_attention.restype = i
         L.attn_selftest_wait_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.attn_selftest_wait_timeout.restype = i
@@ -279,18 +279,22 @@ def sage_attn_fwd_pv16(prep: Prepared, v: torch.Tensor, out: torch.Tensor | None
     return out
 
 
-def sage_attention_workspace(B: int, H: int, S: int, device, smooth_k: bool = False, pv: str = "e4m3") -> torch.Tensor:
-    n = int(lib().sage_attention_workspace_size(B, H, sage_padded_len(S), int(smooth_k), int(pv == "bf16")))
+def sage_attention_workspace(B: int, H: int, S: int, device, smooth_k: bool = False, pv: str = "e4m3",
+                             q_on_load: bool = False) -> torch.Tensor:
+    n = int(lib().sage_attention_workspace_size(B, H, sage_padded_len(S), int(smooth_k), int(pv == "bf16"),
+                                                int(bool(q_on_load))))
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
                    rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3",
-                   workspace=None) -> torch.Tensor:
+                   workspace=None, q_on_load=False) -> torch.Tensor:
     """Prepare + attention in one library call: the SageAttention-style forward of BF16 Q/K/V.
 
     pv="e4m3": P and V in FP8; pv="bf16": P in BF16 times the unquantised V.  The
-    prepared tensors stay in `workspace` (allocated here unless given)."""
+    prepared tensors stay in `workspace` (allocated here unless given).  q_on_load:
+    Q is coded by the forward as it loads it instead of by the prepare (the same
+    output; slower on a GB300)."""
     if pv not in ("e4m3", "bf16"):
         raise ValueError(f"pv must be 'e4m3' or 'bf16', not {pv!r}")
     B, S, H, D = q.shape
@@ -299,7 +303,7 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
     if out is None:
         out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q.device)
     if workspace is None:
-        workspace = sage_attention_workspace(B, H, S, q.device, smooth_k, pv)
+        workspace = sage_attention_workspace(B, H, S, q.device, smooth_k, pv, q_on_load)
     qs, ks, vs, os_ = _bshd("q", q), _bshd("k", k), _bshd("v", v), _bshd("out", out)
 
     def ptr(t):
@@ -308,7 +312,7 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
     _check(lib().sage_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                                 float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
                                 ptr(rope_sin), int(rope_dim), int(bool(smooth_k)), int(pv == "bf16"),
-                                out.data_ptr(), os_, workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+                                int(bool(q_on_load)), out.data_ptr(), os_, workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
     return out
 
 

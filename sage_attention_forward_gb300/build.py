@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsageattn.so")
 SOURCES = ["api.cu", "attn_fwd.cu", "sage_prepare.cu"]
-HEADERS = ["ptx.cuh", "kernels.h"]
+HEADERS = ["ptx.cuh", "kernels.h", "qk_quant.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

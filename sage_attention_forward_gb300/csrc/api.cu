@@ -504,10 +504,12 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
 }
 
 // Workspace of sage_attention: consecutive 256-byte aligned pieces.
+// The one-call op's workspace: Q's FP16 codes and scales (unless the forward codes Q
+// as it loads it), K's, V's codes and scales (FP8 mode), the smoothing buffers.
 struct FusedLayout {
-  size_t q16, k16, q_scale, k_scale, v_fp8, v_scale, vmax, k_mean, k_partial, total;
+  size_t q16, q_scale, k16, k_scale, v_fp8, v_scale, vmax, k_mean, k_partial, total;
 };
-static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16) {
+static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16, int q_on_load) {
   FusedLayout L{};
   const size_t bh = (size_t)B * (size_t)H, nblk = (size_t)(S_pad / 32);
   size_t off = 0;
@@ -516,9 +518,11 @@ static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int p
     off += (bytes + 255) & ~size_t(255);
     return at;
   };
-  L.q16 = take(bh * (size_t)S_pad * 128 * 2);
+  if (!q_on_load) {
+    L.q16 = take(bh * (size_t)S_pad * 128 * 2);
+    L.q_scale = take(bh * nblk * 4);
+  }
   L.k16 = take(bh * (size_t)S_pad * 128 * 2);
-  L.q_scale = take(bh * nblk * 4);
   L.k_scale = take(bh * nblk * 4);
   if (!pv_bf16) {
     L.v_fp8 = take(bh * 128 * (size_t)S_pad);
@@ -533,22 +537,23 @@ static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int p
   return L;
 }
 
-size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16) {
+size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16, int q_on_load) {
   if (B < 1 || H < 1 || S_pad < 1) return 0;
-  return fused_layout(B, H, S_pad, smooth_k, pv_bf16).total;
+  return fused_layout(B, H, S_pad, smooth_k, pv_bf16, q_on_load).total;
 }
 
 attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                            float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
                            const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_k, int pv_bf16,
-                           void* o, const int64_t o_str[3], void* workspace, size_t workspace_bytes,
+                           int q_on_load, void* o, const int64_t o_str[3], void* workspace, size_t workspace_bytes,
                            attn_stream_t stream) {
   bool empty = false;
   TRY(check_shape(B, S, H, D, &empty));
   if (empty) return ATTN_OK;
-  if ((smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1))
-    return fail(ATTN_ERR_INVALID_ARG, "smooth_k=%d and pv_bf16=%d must be 0 or 1", smooth_k, pv_bf16);
+  if ((smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1) || (q_on_load != 0 && q_on_load != 1))
+    return fail(ATTN_ERR_INVALID_ARG, "smooth_k=%d, pv_bf16=%d and q_on_load=%d must be 0 or 1", smooth_k, pv_bf16,
+                q_on_load);
   const int64_t S_pad = sage_padded_len(S);
   sa::PrepareArgs a;
   TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
@@ -557,16 +562,19 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
   TRY(check_strides("o", o, o_str, B, S, H, os));
   if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
   if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
-  const FusedLayout L = fused_layout(B, H, S_pad, smooth_k, pv_bf16);
+  const FusedLayout L = fused_layout(B, H, S_pad, smooth_k, pv_bf16, q_on_load);
   if (workspace_bytes < L.total)
     return fail(ATTN_ERR_INVALID_ARG, "sage_attention: workspace_bytes=%zu < %zu required", workspace_bytes, L.total);
   TRY(check_device());
   TRY(get_encoder());
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  a.q16 = ws + L.q16;
+  if (!q_on_load) {
+    a.q16 = ws + L.q16;
+    a.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
+  }
   a.k16 = ws + L.k16;
-  a.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
   a.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
+  a.skip_q = q_on_load != 0;  // else the forward codes Q as it loads it
   a.skip_v = pv_bf16 != 0;
   if (!pv_bf16) {
     a.v_fp8 = ws + L.v_fp8;
@@ -581,16 +589,37 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
   if (e != cudaSuccess) return fail_cuda(e, "sage_attention prepare");
   const long long bh = (long long)B * H;
   CUtensorMap tq, tk, tv;
-  TRY(tmap_f16_rows(&tq, a.q16, S_pad, bh));
   TRY(tmap_f16_rows(&tk, a.k16, S_pad, bh));
+  if (!q_on_load) {
+    TRY(tmap_f16_rows(&tq, a.q16, S_pad, bh));
+    if (pv_bf16) {
+      TRY(tmap_bhsd_bf16(&tv, v, B, S, H, a.str[2]));
+      e = sa::launch_sage_attn_pv16(tq, tk, tv, a.q_scale, a.k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                    (cudaStream_t)stream);
+    } else {
+      TRY(tmap_bytes_3d(&tv, a.v_fp8, S_pad, 128, bh));
+      e = sa::launch_sage_attn(tq, tk, tv, a.q_scale, a.k_scale, a.v_scale, o, os[0], os[1], os[2], B, S, H,
+                               S_pad, (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "sage_attention launch");
+    return ATTN_OK;
+  }
+  TRY(tmap_bhsd_bf16(&tq, q, B, S, H, a.str[0]));
+  sa::QLoadArgs qa;
+  qa.q_norm_w = a.q_norm_w;
+  qa.rms_eps = a.rms_eps;
+  qa.rope_cos = a.rope_cos;
+  qa.rope_sin = a.rope_sin;
+  qa.rope_dim = a.rope_dim;
+  qa.c_log2 = a.c_log2;
   if (pv_bf16) {
     TRY(tmap_bhsd_bf16(&tv, v, B, S, H, a.str[2]));
-    e = sa::launch_sage_attn_pv16(tq, tk, tv, a.q_scale, a.k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
-                                  (cudaStream_t)stream);
+    e = sa::launch_sage_attn_pv16_qload(tq, tk, tv, qa, a.k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                        (cudaStream_t)stream);
   } else {
     TRY(tmap_bytes_3d(&tv, a.v_fp8, S_pad, 128, bh));
-    e = sa::launch_sage_attn(tq, tk, tv, a.q_scale, a.k_scale, a.v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
-                             (cudaStream_t)stream);
+    e = sa::launch_sage_attn_qload(tq, tk, tv, qa, a.k_scale, a.v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                   (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return fail_cuda(e, "sage_attention launch");
   return ATTN_OK;

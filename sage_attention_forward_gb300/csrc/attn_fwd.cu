@@ -47,6 +47,15 @@
 // softmax warpgroup's wait for its S tile) poll; the producer's and the
 // O-rescale waits sleep on their barriers, which gives their issue slots to
 // the softmax warps.
+//
+// Quantise-on-load of Q (kQLoad, the two Sage modes): the producer loads BF16 Q
+// as the BF16 mode does, and each softmax thread turns its own row into the
+// FP16 codes in place (RMSNorm and RoPE first when asked), with the arithmetic
+// of qk_quant.cuh that the prepare uses, so the codes and the row's scale are
+// the ones the prepare would have written.  One warp's 32 rows are one scale
+// block, whose maximum is a warp reduction.  Each thread then makes its writes
+// visible to the tensor core's proxy and arrives on q_ready[i], which the MMA
+// warp waits on before Q_i's first product.  Q then never reaches HBM as codes.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -54,6 +63,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "qk_quant.cuh"
 
 namespace sa {
 namespace {
@@ -106,6 +116,7 @@ struct __align__(1024) Smem {
   uint64_t p_full[kNQ][2];   // P_i keys [0,64) and [64,128) stored in TMEM
   uint64_t o_done[kNQ];
   uint64_t mma_drain;
+  uint64_t q_ready[kNQ];     // quantise-on-load: all 128 rows of Q_i coded in place
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -124,12 +135,114 @@ struct Params {
   int nblk;               // S_pad / 32
   int n_tiles;            // ceil(S / 128)
   int withhold_loads;     // self-test of the failure path: the producer loads nothing
+  // quantise-on-load of Q
+  const __nv_bfloat16* q_norm_w;   // [128] or nullptr
+  float rms_eps;
+  const __nv_bfloat16* rope_cos;   // [S, rope_dim] or nullptr
+  const __nv_bfloat16* rope_sin;
+  int rope_dim;
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
-template <Mode kMode>
+// Rotate-half RoPE on a whole 128-channel row held as 64 packed BF16 pairs, kHalf =
+// rope_dim / 2 (a compile-time constant so that the pair indices stay in registers).
+template <int kHalf>
+__device__ __forceinline__ void rope_row(uint32_t (&x)[64], const __nv_bfloat16* cs, const __nv_bfloat16* sn) {
+  constexpr int kW = kHalf / 2;   // packed pairs per half
+  const uint4* c4 = reinterpret_cast<const uint4*>(cs);
+  const uint4* s4 = reinterpret_cast<const uint4*>(sn);
+#pragma unroll
+  for (int w4 = 0; w4 < kW / 4; ++w4) {
+    const uint4 cl = __ldg(c4 + w4), ch = __ldg(c4 + kW / 4 + w4);
+    const uint4 sl = __ldg(s4 + w4), sh = __ldg(s4 + kW / 4 + w4);
+    const uint32_t clo[4] = {cl.x, cl.y, cl.z, cl.w}, chi[4] = {ch.x, ch.y, ch.z, ch.w};
+    const uint32_t slo[4] = {sl.x, sl.y, sl.z, sl.w}, shi[4] = {sh.x, sh.y, sh.z, sh.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int w = 4 * w4 + e;
+      const uint32_t lo = x[w], hi = x[w + kW];
+      x[w] = qk::rope_first_half(lo, hi, clo[e], slo[e]);
+      x[w + kW] = qk::rope_second_half(hi, lo, chi[e], shi[e]);
+    }
+    // keeps the next group's table loads from being hoisted above this group's arithmetic,
+    // which would hold every table word of the row in registers at once
+    asm volatile("" ::: "memory");
+  }
+}
+
+// Quantise-on-load: the calling thread's row `row` of a BF16 Q tile (two [128][64]
+// halves, 128-byte swizzle) becomes its FP16 codes in place; returns the row's score
+// factor (its 32-row block's scale, softmax_scale * log2 e included).  The whole warp
+// calls it: its 32 rows are one block.  grow = the row's position in the sequence.
+__device__ __noinline__ float quantise_q_row(uint8_t* qtile, int row, int grow, const Params& p, float c_log2) {
+  uint32_t x[64];
+  uint8_t* const rp = qtile + row * 128;   // the row in the first half; the second is kHalfBytes on
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(rp + hf * kHalfBytes + ((c ^ (row & 7)) << 4));
+      x[32 * hf + 4 * c + 0] = v.x;
+      x[32 * hf + 4 * c + 1] = v.y;
+      x[32 * hf + 4 * c + 2] = v.z;
+      x[32 * hf + 4 * c + 3] = v.w;
+    }
+  if (p.q_norm_w != nullptr) {
+    float P[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) P[g] = qk::sumsq16(&x[8 * g]);
+    const float r = qk::rms_factor(qk::sumsq_combine(P), p.rms_eps);
+    const uint4* w4 = reinterpret_cast<const uint4*>(p.q_norm_w);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 w = __ldg(w4 + c);
+      x[4 * c + 0] = qk::rms_apply(x[4 * c + 0], r, w.x);
+      x[4 * c + 1] = qk::rms_apply(x[4 * c + 1], r, w.y);
+      x[4 * c + 2] = qk::rms_apply(x[4 * c + 2], r, w.z);
+      x[4 * c + 3] = qk::rms_apply(x[4 * c + 3], r, w.w);
+    }
+  }
+  if (grow >= p.S) {
+    // rows past S are zeros (with rms_eps = 0 their RMSNorm factor is infinite) and code to 0
+#pragma unroll
+    for (int w = 0; w < 64; ++w) x[w] = 0u;
+  } else if (p.rope_dim > 0) {
+    const __nv_bfloat16* cs = p.rope_cos + (long long)grow * p.rope_dim;
+    const __nv_bfloat16* sn = p.rope_sin + (long long)grow * p.rope_dim;
+    switch (p.rope_dim) {
+      case 32: rope_row<16>(x, cs, sn); break;
+      case 64: rope_row<32>(x, cs, sn); break;
+      case 96: rope_row<48>(x, cs, sn); break;
+      default: rope_row<64>(x, cs, sn); break;
+    }
+  }
+  uint32_t m2 = 0u;
+#pragma unroll
+  for (int w = 0; w < 64; ++w) m2 = qk::bf2_max(m2, qk::bf2_abs(x[w]));
+  float a = fmaxf(qk::bf_lo(m2), qk::bf_hi(m2));
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+  const float inv = qk::code_factor(a);
+  auto emit = [&](auto kClamp) {
+    constexpr bool kC = decltype(kClamp)::value;
+#pragma unroll
+    for (int w = 0; w < 64; ++w)
+      x[w] = qk::codes_fp16x2(qk::code_magic<kC>(qk::bf_lo(x[w]), inv), qk::code_magic<kC>(qk::bf_hi(x[w]), inv));
+  };
+  if (isinf(inv)) emit(std::true_type{});   // warp-uniform: 127 / a overflowed
+  else emit(std::false_type{});
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(rp + hf * kHalfBytes + ((c ^ (row & 7)) << 4)) =
+          make_uint4(x[32 * hf + 4 * c], x[32 * hf + 4 * c + 1], x[32 * hf + 4 * c + 2], x[32 * hf + 4 * c + 3]);
+  return qk::block_scale(a, c_log2, true);
+}
+
+template <Mode kMode, bool kQLoad>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -165,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.o_done[i], 1);
     }
     mbar_init(&sm.mma_drain, 1);
+    for (int i = 0; i < kNQ; ++i) mbar_init(&sm.q_ready[i], 4 * 32);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -189,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kNQ; ++i)
         for (int hf = 0; hf < 2; ++hf) {
           // rows past S read as 0 (their output is not stored)
-          if constexpr (kInt8)
+          if constexpr (kInt8 && !kQLoad)
             tma_load_3d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh);
           else
             tma_load_4d(sm.q[i] + hf * kHalfBytes, &tm_q, &sm.q_full, hf * 64, q_row0 + i * kBM, bh % p.H,
@@ -300,12 +414,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
-      bool ok = mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      // Q_i is ready when its tile has landed, or with quantise-on-load when its 128 softmax
+      // threads have coded it in place
+      auto wait_q = [&](int i) -> bool {
+        if constexpr (kQLoad) return mbar_wait_warp<false>(&sm.q_ready[i], 0, abort_flag, err, kErrTimeoutSync);
+        else return i > 0 || mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      };
+      bool ok = wait_q(0);
       if (ok) ok = mbar_wait_warp<false>(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         if (leader) mma_commit(&sm.s_full[0]);
+        ok = wait_q(1);
+      }
+      if (ok) {
+        tc_fence_after();
         issue_s(1, 0);
         if (leader) mma_commit(&sm.s_full[1]);
         if (leader) mma_commit(&sm.k_empty[0]);
@@ -364,26 +488,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
+    uint32_t* err = &g_err_attn;
+    bool ok = true;
+    // score factors: Sage modes, the row's Q scale (it carries softmax_scale * log2 e; rows
+    // past S use the slot of a real block) times each 32-key block's K scale; BF16 mode, c
+    float qs = p.c_log2;
+    if constexpr (kQLoad) {
+      // first, before the rest of the row's state exists: code the row in place
+      ok = mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) {
+        qs = quantise_q_row(sm.q[i], row, q_row0 + i * kBM + row, p, p.c_log2);
+        // the codes are read by the tensor core (the async proxy) once all 128 rows are in
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.q_ready[i]);
+      }
+    }
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128u * i;
     const uint32_t tO = tmem + lane_off + 256u + 128u * i;
     const int grow = q_row0 + i * kBM + row;
-    // score factors: Sage modes, the row's Q scale (it carries softmax_scale * log2 e; rows
-    // past S use the slot of a real block) times each 32-key block's K scale; BF16 mode, c
-    float qs = p.c_log2;
     const float* ksp = nullptr;
     float4 ks_next = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
     if constexpr (kInt8) {
-      const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
-      qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
+      if constexpr (!kQLoad) {
+        const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
+        qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
+      }
       ksp = p.k_scale + (long long)bh * p.nblk;
       ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
     }
-    uint32_t* err = &g_err_attn;
     float m_used = -INFINITY, l = 0.0f;
-    bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; ok && j < n; ++j) {
       // K scales of the tile's four 32-key blocks: prefetched a tile ahead in the FP8 mode;
       // the 16-bit mode, whose BF16 P takes twice the registers, loads them when needed
       float4 ks4 = ks_next;
@@ -612,18 +748,18 @@ size_t smem_bytes_of() {
   return sizeof(Smem<kMode>) + 1024;
 }
 
-template <Mode kMode>
+template <Mode kMode, bool kQLoad = false>
 cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const float* q_scale, const float* k_scale, const float* v_scale, float c_log2, void* o,
                           long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
-                          cudaStream_t stream, bool withhold_loads = false) {
+                          cudaStream_t stream, bool withhold_loads = false, const QLoadArgs* qa = nullptr) {
   static bool attr_done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   const size_t smem = smem_bytes_of<kMode>();
   if (!attr_done[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(attn_fwd_kernel<kMode, kQLoad>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -641,8 +777,20 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   p.nblk = (int)(S_pad / 32);
   p.n_tiles = (S + kBN - 1) / kBN;
   p.withhold_loads = withhold_loads ? 1 : 0;
+  p.q_norm_w = nullptr;
+  p.rms_eps = 0.0f;
+  p.rope_cos = p.rope_sin = nullptr;
+  p.rope_dim = 0;
+  if (qa != nullptr) {
+    p.q_norm_w = reinterpret_cast<const __nv_bfloat16*>(qa->q_norm_w);
+    p.rms_eps = qa->rms_eps;
+    p.rope_cos = reinterpret_cast<const __nv_bfloat16*>(qa->rope_cos);
+    p.rope_sin = reinterpret_cast<const __nv_bfloat16*>(qa->rope_sin);
+    p.rope_dim = qa->rope_dim;
+    p.c_log2 = qa->c_log2;
+  }
   dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
-  attn_fwd_kernel<kMode><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
+  attn_fwd_kernel<kMode, kQLoad><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 
@@ -677,6 +825,22 @@ cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& 
                                   long long S_pad, cudaStream_t stream) {
   return launch_kernel<Mode::kSagePV16>(tm_q16, tm_k16, tm_v_bf16, q_scale, k_scale, nullptr, 0.0f, o, o_sb, o_ss,
                                         o_sh, B, S, H, S_pad, stream);
+}
+
+cudaError_t launch_sage_attn_qload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k16,
+                                   const CUtensorMap& tm_v8, const QLoadArgs& qa, const float* k_scale,
+                                   const float* v_scale, void* o, long long o_sb, long long o_ss, long long o_sh,
+                                   int B, int S, int H, long long S_pad, cudaStream_t stream) {
+  return launch_kernel<Mode::kSageFP8, true>(tm_q_bf16, tm_k16, tm_v8, nullptr, k_scale, v_scale, 0.0f, o, o_sb,
+                                             o_ss, o_sh, B, S, H, S_pad, stream, false, &qa);
+}
+
+cudaError_t launch_sage_attn_pv16_qload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k16,
+                                        const CUtensorMap& tm_v_bf16, const QLoadArgs& qa, const float* k_scale,
+                                        void* o, long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                        long long S_pad, cudaStream_t stream) {
+  return launch_kernel<Mode::kSagePV16, true>(tm_q_bf16, tm_k16, tm_v_bf16, nullptr, k_scale, nullptr, 0.0f, o,
+                                              o_sb, o_ss, o_sh, B, S, H, S_pad, stream, false, &qa);
 }
 
 cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,

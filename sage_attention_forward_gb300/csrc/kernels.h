@@ -45,6 +45,7 @@ struct PrepareArgs {
   void* q16 = nullptr;       // when set: Q/K codes written as FP16 [B*H, S_pad, 128] here, not as INT8
   void* k16 = nullptr;
   bool skip_v = false;       // V not prepared (the 16-bit P V mode reads the BF16 input)
+  bool skip_q = false;       // Q not prepared (the forward quantises Q as it loads it)
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 
@@ -66,5 +67,25 @@ cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& 
                                   const CUtensorMap& tm_v_bf16, const float* q_scale, const float* k_scale, void* o,
                                   long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
                                   long long S_pad, cudaStream_t stream);
+
+// Quantise-on-load of Q: the forward reads BF16 Q through a [B, S, H, 128] tensor
+// map and each softmax thread turns its own row into the codes and the scale the
+// prepare would have written (optional RMSNorm + RoPE first, the same arithmetic).
+struct QLoadArgs {
+  const void* q_norm_w = nullptr;   // BF16 [128], or nullptr: no RMSNorm
+  float rms_eps = 0.0f;
+  const void* rope_cos = nullptr;   // BF16 [S, rope_dim], or nullptr: no RoPE
+  const void* rope_sin = nullptr;
+  int rope_dim = 0;
+  float c_log2 = 0.0f;              // fl32(softmax_scale * log2 e), folded into Q's scales
+};
+cudaError_t launch_sage_attn_qload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k16,
+                                   const CUtensorMap& tm_v8, const QLoadArgs& qa, const float* k_scale,
+                                   const float* v_scale, void* o, long long o_sb, long long o_ss, long long o_sh,
+                                   int B, int S, int H, long long S_pad, cudaStream_t stream);
+cudaError_t launch_sage_attn_pv16_qload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k16,
+                                        const CUtensorMap& tm_v_bf16, const QLoadArgs& qa, const float* k_scale,
+                                        void* o, long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                        long long S_pad, cudaStream_t stream);
 
 }  // namespace sa

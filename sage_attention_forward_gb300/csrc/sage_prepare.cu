@@ -7,20 +7,13 @@
 // inputs, and the order of the one order-dependent sum (RMSNorm's sum of
 // squares) is fixed below.
 //
-// Instruction selection keeps the instruction count low while every result
-// stays that of the rounded operation it implements: BF16 roundings of binary32
-// values go in pairs (cvt.rn.bf16x2.f32, which also packs the pair for the next
-// stage); a BF16 x BF16 product or BF16 + BF16 sum that eager arithmetic rounds
-// from binary32 is one mul/add.rn.bf16x2 (the same value, see bf2_mul); the RoPE
-// term -partner*sin is the rounded partner*sin with its sign bits flipped
-// (rounding to nearest even is sign-symmetric); block maxima of |BF16| values
-// are taken on the packed pairs (max.bf16x2); and the INT8 code
-// clamp(rne(v * inv), -127, 127) is formed as v * inv + 1.5 * 2^23, whose
-// addition rounds to the integer and leaves it in the low mantissa bits.
-// (NaN, which only RMSNorm of an all-zero or underflowing row with rms_eps = 0
-// produces, has no defined code.)
+// The per-element arithmetic (the RMSNorm factor and scaling, the RoPE pair, the
+// codes and scales) is that of qk_quant.cuh, which the attention kernel's
+// quantise-on-load of Q uses too, so both produce the same codes.  (NaN, which
+// only RMSNorm of an all-zero or underflowing row with rms_eps = 0 produces, has
+// no defined code.)
 //
-// Kernel 1 (grid.z = 0: Q, 1: K, 2: V maxima) -- one warp per (b, h, 32-row
+// Kernel 1 (tasks Q, K, V maxima over grid.z; Q or V may be skipped) -- one warp per (b, h, 32-row
 // block).  A row of 128 channels is held by 8 lanes, lane L of the group owning
 // channels [16L, 16L + 16) (two 128-bit loads); a warp covers 4 rows per step
 // and 32 rows in 8 steps, so every lane keeps 8 rows x 16 channels in
@@ -42,6 +35,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "qk_quant.cuh"
 
 namespace sa {
 namespace {
@@ -63,10 +57,11 @@ struct QKParams {
   float c_log2;                     // fl32(softmax_scale * log2 e), folded into Q's scales
   uint32_t* vmax;                   // [B*H*128] float bits of the channel maxima of |V|
   const float* kmean;               // [B*H*128] K smoothing: subtracted from K before quantising (or nullptr)
+  int task0;                        // task of grid.z = 0 (1 when Q is skipped)
 };
 
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+using namespace qk;
+
 __device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&f)[16]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -74,38 +69,6 @@ __device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&f)[16])
     f[2 * i + 1] = bf_hi(w[i]);
   }
 }
-// Two floats rounded to BF16 (nearest even) by one paired conversion; the result
-// holds lo in its low half, as the [.., 128] rows store channel pairs.
-__device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-// Products and sums of two BF16 values, rounded once to BF16 (mul/add.rn.bf16x2).
-// Eager BF16 arithmetic computes them in binary32 and rounds that to BF16; the two
-// agree for all finite operands.  A product of two 8-bit significands is exact in
-// binary32 down to 2^-149, and below that it lies under the smallest BF16 rounding
-// midpoint (2^-134) either way.  A sum is exact in binary32 unless the exponents
-// differ by more than 15, and then the smaller term is far below half a BF16 ulp
-// of the larger, so both roundings return the larger.
-__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-// Per-half maximum of two BF16 pairs (max.bf16x2).
-__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-// 1.5 * 2^23: for |v| < 2^22, v + kRoundMagic is rounded to an integer (nearest even) by the
-// addition itself, and that integer n is stored in the low mantissa bits: bits = 0x4B400000 + n.
-constexpr float kRoundMagic = 12582912.0f;
 __device__ __forceinline__ void load16(const __nv_bfloat16* src, uint32_t (&w)[8]) {
   const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
   const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
@@ -141,34 +104,26 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
   if (nw != nullptr) {
     uint32_t ww[8];
     load16(nw + 16 * L, ww);
-    // the sum of squares of each row (the same order in every lane of the row's group);
+    // the sum of squares of each row: 16-channel partials combined by an XOR butterfly (the
+    // order of sumsq_combine, the same value in every lane of the row's group);
     // lane L of a group keeps the sum of its step-L row, takes 1 / sqrt(mean + eps) of it
     // once, and the group's lanes fetch each step's factor from lane L = step by a shuffle
     float mine = 0.0f;
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        // unpacked by byte permutes, not the shifts the scaling below uses, so that the
-        // compiler recomputes them there instead of holding 128 floats across the shuffles
-        const float lo = __uint_as_float(__byte_perm(x[step][i], 0u, 0x1044));
-        const float hi = __uint_as_float(__byte_perm(x[step][i], 0u, 0x3244));
-        acc = __fadd_rn(acc, __fmul_rn(lo, lo));
-        acc = __fadd_rn(acc, __fmul_rn(hi, hi));
-      }
+      float acc = sumsq16(x[step]);
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
       mine = (L == step) ? acc : mine;
     }
-    const float r_mine = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(mine, 1.0f / 128.0f), p.eps)));
+    const float r_mine = rms_factor(mine, p.eps);
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
       const float r = __shfl_sync(0xffffffffu, r_mine, (lane & ~7) | step);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        x[step][i] = bf2_mul(bf2_bits(__fmul_rn(bf_lo(x[step][i]), r), __fmul_rn(bf_hi(x[step][i]), r)), ww[i]);
+        x[step][i] = rms_apply(x[step][i], r, ww[i]);
     }
     // rows >= S stay exact zeros (with rms_eps = 0 their factor is infinite); only the last
     // block has such rows
@@ -200,8 +155,7 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
         uint32_t cw[8], sw[8];
         load16(p.rope_cos + (long long)s * p.rope_dim + 16 * L, cw);
         load16(p.rope_sin + (long long)s * p.rope_dim + 16 * L, sw);
-        // x*cos + rot*sin with rot = -partner on the low half: round(-u) = -round(u) under
-        // nearest-even rounding, so the rounded partner*sin pair has its signs flipped instead
+        // rope_first_half / rope_second_half, the half chosen per lane by the sign mask
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           x[step][i] = bf2_add(bf2_mul(x[step][i], cw[i]), bf2_mul(partner[i], sw[i]) ^ neg);
@@ -211,8 +165,8 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
 
 }
 
-__global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
-  const int task = blockIdx.z;
+__global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) {
+  const int task = blockIdx.z + p.task0;
   const int bh = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -236,7 +190,7 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
           uint32_t w[8];
           load16(base + (long long)s * ss, w);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m2[i] = bf2_max(m2[i], w[i] & 0x7fff7fffu);
+          for (int i = 0; i < 8; ++i) m2[i] = bf2_max(m2[i], bf2_abs(w[i]));
         }
       }
     }
@@ -292,60 +246,44 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
 #pragma unroll
     for (int step = 0; step < 8; ++step)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m2 = bf2_max(m2, x[step][i] & 0x7fff7fffu);
+      for (int i = 0; i < 8; ++i) m2 = bf2_max(m2, bf2_abs(x[step][i]));
     a = fmaxf(bf_lo(m2), bf_hi(m2));
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
-  const float inv = (a > 0.0f) ? __fdiv_rn(127.0f, a) : 0.0f;
+  const float inv = code_factor(a);
   int8_t* out = p.codes[task] + ((long long)bh * p.S_pad) * 128 + 16 * L;
   __half* out16 = p.codes16[task] ? p.codes16[task] + ((long long)bh * p.S_pad) * 128 + 16 * L : nullptr;
-  // code = clamp(round_nearest_even(v * inv), -127, 127), the rounding done by adding
-  // kRoundMagic to v * inv clamped to [-127, 127] (the same integer).  With a finite inv the
-  // clamp never binds: |v| <= a, so |v * inv| <= 127 (1 + 2^-24) before rounding, which rounds
-  // to 127.  Only when 127 / a overflows (a whole block below 3.7e-37) is it needed; the
-  // block is one warp's, so the choice is warp-uniform.  Rows >= S code to 0.
+  // codes by code_magic; its clamp only where 127 / a overflowed, a warp-uniform choice (the
+  // block is one warp's)
   auto emit_codes = [&](auto kClamp, auto kSmooth) {
+    constexpr bool kC = decltype(kClamp)::value;
 #pragma unroll
     for (int step = 0; step < 8; ++step) {
       const int s = 32 * blk + 4 * step + g;
       const bool live = s < p.S;
       auto code = [&](float f, int i) {
         if constexpr (decltype(kSmooth)::value) {
-          float v = __fmul_rn(__fsub_rn(f, mu[i]), inv);
-          if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
-          return live ? __fadd_rn(v, kRoundMagic) : kRoundMagic;
+          return live ? code_magic<kC>(__fsub_rn(f, mu[i]), inv) : kRoundMagic;
         } else {
-          // rows >= S hold zeros here, which code to 0
-          float v = __fmul_rn(f, inv);
-          if constexpr (decltype(kClamp)::value) v = fminf(fmaxf(v, -127.0f), 127.0f);
-          return __fadd_rn(v, kRoundMagic);
+          return code_magic<kC>(f, inv);   // rows >= S hold zeros here, which code to 0
         }
       };
       if (out16) {
-        // the same codes as FP16, exact (|code| <= 127): the operand the attention kernel's
-        // Q K^T MMA reads
+        // the same codes as FP16, exact: the operand the attention kernel's Q K^T MMA reads
         uint32_t hw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float y0 = code(bf_lo(x[step][i]), 2 * i), y1 = code(bf_hi(x[step][i]), 2 * i + 1);
-          const __half2 hv = __floats2half2_rn(__fsub_rn(y0, kRoundMagic), __fsub_rn(y1, kRoundMagic));
-          hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
+        for (int i = 0; i < 8; ++i)
+          hw[i] = codes_fp16x2(code(bf_lo(x[step][i]), 2 * i), code(bf_hi(x[step][i]), 2 * i + 1));
         uint4* d = reinterpret_cast<uint4*>(out16 + (long long)s * 128);
         d[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         d[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
       } else {
-        // the code's two's-complement byte is the low byte of its kRoundMagic sum
         uint32_t q[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t lo = __byte_perm(__float_as_uint(code(bf_lo(x[step][2 * w]), 4 * w)),
-                                          __float_as_uint(code(bf_hi(x[step][2 * w]), 4 * w + 1)), 0x0040);
-          const uint32_t hi = __byte_perm(__float_as_uint(code(bf_lo(x[step][2 * w + 1]), 4 * w + 2)),
-                                          __float_as_uint(code(bf_hi(x[step][2 * w + 1]), 4 * w + 3)), 0x0040);
-          q[w] = __byte_perm(lo, hi, 0x5410);
-        }
+        for (int w = 0; w < 4; ++w)
+          q[w] = codes_int8x4(code(bf_lo(x[step][2 * w]), 4 * w), code(bf_hi(x[step][2 * w]), 4 * w + 1),
+                              code(bf_lo(x[step][2 * w + 1]), 4 * w + 2), code(bf_hi(x[step][2 * w + 1]), 4 * w + 3));
         *reinterpret_cast<uint4*>(out + (long long)s * 128) = make_uint4(q[0], q[1], q[2], q[3]);
       }
     }
@@ -357,14 +295,7 @@ __global__ void __launch_bounds__(256) prep_qk_vmax_kernel(const QKParams p) {
     if (isinf(inv)) emit_codes(std::true_type{}, std::false_type{});
     else emit_codes(std::false_type{}, std::false_type{});
   }
-  if (lane == 0) {
-    float sc = 0.0f;
-    if (a > 0.0f) {
-      sc = __fdiv_rn(a, 127.0f);
-      if (task == 0) sc = __fmul_rn(sc, p.c_log2);
-    }
-    p.scales[task][(long long)bh * p.nblk + blk] = sc;
-  }
+  if (lane == 0) p.scales[task][(long long)bh * p.nblk + blk] = block_scale(a, p.c_log2, task == 0);
 }
 
 // ------------------------------------------------------------------ K smoothing
@@ -549,6 +480,7 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   p.c_log2 = a.c_log2;
   p.vmax = a.vmax;
   p.kmean = a.k_mean;
+  p.task0 = a.skip_q ? 1 : 0;
   if (a.k_mean != nullptr) {
     dim3 g0((nblk + 7) / 8, a.B * a.H, 1);
     prep_kmean_partial_kernel<<<g0, 256, 0, stream>>>(p, a.k_partial);
@@ -558,7 +490,7 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 g1((nblk + 7) / 8, a.B * a.H, a.skip_v ? 2 : 3);   // grid.z = 2: Q and K only
+  dim3 g1((nblk + 7) / 8, a.B * a.H, (a.skip_v ? 2 : 3) - p.task0);   // tasks [task0, 3 or 2)
   prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

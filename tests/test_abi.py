@@ -143,18 +143,21 @@ def test_selftest_rejects_bad_pointers():
 def test_sage_attention_one_call_rejects_bad_arguments():
     L = sa.lib()
     st = I64x3(256 * 2 * 128, 256, 128)
-    ws = L.sage_attention_workspace_size(1, 2, 256, 0, 0)
+    ws = L.sage_attention_workspace_size(1, 2, 256, 0, 0, 0)
     # FP16 Q and K codes, their scales, e4m3 V^T, V scales and channel maxima, 256-byte pieces
     assert ws == 2 * (2 * 256 * 128 * 2) + 2 * 256 + 2 * 128 * 256 + 1024 + 1024
-    assert L.sage_attention_workspace_size(1, 2, 256, 0, 1) < ws          # no V in the 16-bit mode
-    assert L.sage_attention_workspace_size(1, 2, 256, 1, 0) > ws          # K smoothing adds its sums
+    # Q coded inside the forward: no Q codes or scales
+    assert L.sage_attention_workspace_size(1, 2, 256, 0, 0, 1) == ws - (2 * 256 * 128 * 2) - 256
+    assert L.sage_attention_workspace_size(1, 2, 256, 0, 1, 0) < ws       # no V in the 16-bit mode
+    assert L.sage_attention_workspace_size(1, 2, 256, 1, 0, 0) > ws       # K smoothing adds its sums
 
-    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256):
+    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256, qload=0):
         return L.sage_attention(FAKE, FAKE, FAKE, 1, S, 2, 128, st, st, st, 0.088, None, None, 1e-6, None, None, 0,
-                                smooth, pv, o, st, FAKE, ws_bytes, None)
+                                smooth, pv, qload, o, st, FAKE, ws_bytes, None)
 
     assert call(smooth=2) == 1
     assert call(pv=-1) == 1
+    assert call(qload=3) == 1
     assert call(o=FAKE + 2) == 2
     assert call(ws_bytes=ws - 1) == 1
     assert call(S=0) == 1

@@ -21,7 +21,8 @@ REG_BUDGET_ATTN = 168
 
 def ptxas_report(src, tmp_path):
     """Compile one translation unit with the library's own flags; return
-    {kernel: {"regs": n, "spill": bytes}} from ptxas's statistics."""
+    {function: {"regs": n, "spill": bytes, "entry": bool}} from ptxas's
+    statistics (kernels, and device functions compiled as calls)."""
     out = tmp_path / (os.path.basename(src) + ".o")
     cmd = [lib_build.nvcc()] + lib_build._flags(["-Xptxas", "-v"]) + ["-c", src, "-o", str(out)]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
@@ -31,13 +32,19 @@ def ptxas_report(src, tmp_path):
         m = re.search(r"Compiling entry function '([^']+)'", line)
         if m:
             current = m.group(1)
-            kernels[current] = {"regs": None, "spill": None}
+            kernels[current] = {"regs": None, "spill": None, "entry": True}
+            continue
+        m = re.search(r"Function properties for (\S+)", line)
+        if m:
+            current = m.group(1)
+            # a called function is reported once per kernel that calls it: keep the worst
+            kernels.setdefault(current, {"regs": None, "spill": None, "entry": False})
             continue
         if current is None:
             continue
         m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
         if m:
-            kernels[current]["spill"] = int(m.group(1)) + int(m.group(2))
+            kernels[current]["spill"] = max(kernels[current]["spill"] or 0, int(m.group(1)) + int(m.group(2)))
         m = re.search(r"Used (\d+) registers", line)
         if m:
             kernels[current]["regs"] = int(m.group(1))
@@ -50,10 +57,13 @@ def test_no_kernel_spills(src, tmp_path):
     if src != "api.cu":                              # api.cu holds host entry points
         assert kernels, f"{src}: no kernels in the ptxas report"
     for name, st in kernels.items():
-        assert st["spill"] is not None and st["regs"] is not None, f"{name}: incomplete report {st}"
+        assert st["spill"] is not None, f"{name}: incomplete report {st}"
+        assert st["regs"] is not None or not st["entry"], f"{name}: incomplete report {st}"
         assert st["spill"] == 0, f"{name} spills: {st}"
     if src == "attn_fwd.cu":
-        attn = {n: st for n, st in kernels.items() if "attn_fwd_kernel" in n}
-        assert len(attn) == 3, sorted(attn)          # the BF16, Sage FP8-PV and Sage 16-bit-PV modes
+        attn = {n: st for n, st in kernels.items() if "attn_fwd_kernel" in n and st["entry"]}
+        # the BF16, Sage FP8-PV and Sage 16-bit-PV modes, the two Sage modes also with Q
+        # quantised on load
+        assert len(attn) == 5, sorted(attn)
         for name, st in attn.items():
             assert st["regs"] <= REG_BUDGET_ATTN, f"{name} uses {st['regs']} registers"

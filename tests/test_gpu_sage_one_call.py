@@ -1,14 +1,20 @@
 """sage_attention, the one-call Sage op (CUDA through the C ABI), equals the
 two-call sequence sage_prepare (+ smoothing) + sage_attn_fwd / sage_attn_fwd_pv16
-bit for bit: its prepare writes the same codes, as FP16, straight into the
-workspace the forward reads, and the forward kernel is the same.  (The two-call
-path is checked against the oracle in test_gpu_prepare.py, test_gpu_sage.py,
-test_gpu_sage_pv16.py and test_gpu_smooth_k.py.)"""
+bit for bit: its prepare writes the Q/K codes as FP16 straight into the
+workspace the forward reads and V's as sage_prepare does, and the forward's
+arithmetic from the codes on is the same.  With q_on_load the forward codes Q
+itself as it loads it (RMSNorm and RoPE first when asked); equal outputs then
+pin those in-kernel Q codes and scales to the prepare's, which
+test_gpu_prepare.py pins to the oracle bit for bit.  (The two-call path is checked against the oracle
+in test_gpu_prepare.py, test_gpu_sage.py, test_gpu_sage_pv16.py and
+test_gpu_smooth_k.py.)"""
+import dataclasses
+
 import pytest
 import torch
 
 import sage_attention_forward_gb300 as sa
-from workloads import make_inputs, small_case, to_device
+from workloads import make_inputs, small_case, to_device, wide_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -29,15 +35,16 @@ def two_calls(g, wl, smooth_k, pv):
     return sa.sage_attn_fwd(prep)
 
 
+@pytest.mark.parametrize("q_on_load", [False, True])
 @pytest.mark.parametrize("pv", ["e4m3", "bf16"])
 @pytest.mark.parametrize("smooth_k", [False, True])
 @pytest.mark.parametrize("B,H,S,kw", [(1, 2, 31, {}), (2, 3, 300, dict(k_channel_offset_std=1.0)),
                                       (1, 2, 500, dict(rms_norm=True, rope_dim=64))])
-def test_one_call_equals_two_calls(cuda_dev, B, H, S, kw, smooth_k, pv):
+def test_one_call_equals_two_calls(cuda_dev, B, H, S, kw, smooth_k, pv, q_on_load):
     inp = make_inputs(small_case(B, H, S, 1500 + S, **kw))
     g = to_device(inp, cuda_dev)
     o1 = sa.sage_attention(g.q, g.k, g.v, softmax_scale=inp.wl.softmax_scale, smooth_k=smooth_k, pv=pv,
-                           **kwargs(g, inp.wl))
+                           q_on_load=q_on_load, **kwargs(g, inp.wl))
     o2 = two_calls(g, inp.wl, smooth_k, pv)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
@@ -65,3 +72,62 @@ def test_non_default_stream_and_permuted_output(cuda_dev):
     s.synchronize()
     torch.cuda.synchronize()
     assert torch.equal(store.permute(0, 2, 1, 3), o1)
+
+
+@pytest.mark.parametrize("pv", ["e4m3", "bf16"])
+@pytest.mark.parametrize("rope_dim,norm", [(32, True), (96, True), (128, True), (128, False), (0, True)])
+def test_q_coded_on_load_with_norm_and_rope(cuda_dev, rope_dim, norm, pv):
+    inp = make_inputs(small_case(1, 3, 400, 1600 + rope_dim, rms_norm=norm, rope_dim=rope_dim))
+    g = to_device(inp, cuda_dev)
+    o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, q_on_load=True, **kwargs(g, inp.wl))
+    o2 = two_calls(g, inp.wl, False, pv)
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("S", [129, 300, 513])
+def test_q_coded_on_load_zero_eps_ragged(cuda_dev, S):
+    """rms_eps = 0: the rows past S, zeros whose RMSNorm factor is infinite, code to 0
+    in the forward as in the prepare (also the rows past the padded length)."""
+    wl = dataclasses.replace(small_case(1, 2, S, 1700 + S, rms_norm=True, rope_dim=64), rms_eps=0.0)
+    inp = make_inputs(wl)
+    g = to_device(inp, cuda_dev)
+    o1 = sa.sage_attention(g.q, g.k, g.v, q_on_load=True, **kwargs(g, wl))
+    o2 = two_calls(g, wl, False, "e4m3")
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    assert torch.equal(o1, o2)
+
+
+def test_q_coded_on_load_extreme_blocks(cuda_dev):
+    """Q blocks at the low end of the BF16 range, among them blocks whose 127 / max
+    overflows (every code +-127: the forward's clamped branch) and subnormal ones,
+    next to blocks spanning many binades."""
+    S, H = 256, 2
+    # the largest blocks stay below 2^13, which keeps every score below 2^20 in magnitude (both
+    # kernels form 2^(t - m) with a fused multiply-add, whose residual against the rounded
+    # maximum only stays negligible while |t| is well below 2^24)
+    ranges = [(-130, -123), (-20, 13), (5, 13), (-133, -126), (-3, 3), (-126, -100), (0, 1), (-60, 13)]
+    q = torch.cat([wide_bf16(1800 + i, (1, 32, H, 128), lo, hi) for i, (lo, hi) in enumerate(ranges)], dim=1)
+    inp = make_inputs(small_case(1, H, S, 1810))
+    inp.q = q
+    g = to_device(inp, cuda_dev)
+    for pv in ("e4m3", "bf16"):
+        o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, q_on_load=True)
+        o2 = two_calls(g, inp.wl, False, pv)
+        torch.cuda.synchronize()
+        sa.attn_get_device_status()
+        assert torch.equal(o1, o2), pv
+
+
+@pytest.mark.parametrize("name", ["flux2048", "hunyuan720p"])
+def test_q_coded_on_load_workloads(cuda_dev, workload_inputs, name):
+    """FLUX-2048 (RMSNorm + RoPE 64 on Q) and HunyuanVideo-720p (head-major Q
+    strides) at full size."""
+    cpu, g = workload_inputs(name)
+    o1 = sa.sage_attention(g.q, g.k, g.v, softmax_scale=cpu.wl.softmax_scale, q_on_load=True, **kwargs(g, cpu.wl))
+    o2 = two_calls(g, cpu.wl, False, "e4m3")
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    assert torch.equal(o1, o2)
