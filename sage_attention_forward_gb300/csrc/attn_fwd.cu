@@ -548,7 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32_max(tS + 64, s2, r2);
       tmem_ld32_max(tS + 96, s3, r3);
       // scales are >= 0, so a key block's largest t is f * (largest raw score); a block
-      // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores
+      // with no valid key gives -inf * f (NaN when f = 0), which fmaxf ignores.  (The exponent
+      // argument below is the fused s * f - m against this rounded maximum; their difference
+      // for the maximal key is a rounding of t, negligible while |t| is far below 2^24.)
       if (valid >= kBN) {
         const float m01 = fmaxf(r0 * f[0], r1 * f[1]);
         tmem_ld_wait();

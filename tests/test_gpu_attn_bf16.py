@@ -15,7 +15,7 @@ import torch
 import oracle
 import sage_attention_forward_gb300 as sa
 from parity import BF16_A, BF16_B, assert_bf16_gate, gather_rows, metrics
-from workloads import make_inputs, sample_rows, small_case, to_device, WORKLOADS
+from workloads import make_inputs, sample_rows, small_case, to_device, wide_bf16, WORKLOADS
 
 pytestmark = pytest.mark.gpu
 
@@ -116,3 +116,19 @@ def test_other_softmax_scale(cuda_dev):
 
 def test_device_status_is_clean(cuda_dev):
     sa.attn_get_device_status()
+
+
+def test_saturated_softmax_large_logits(cuda_dev):
+    """Query rows scaled by 2^4 to 2^10 next to ordinary ones: logits up to ~2000 (log2
+    units), a softmax that is one-hot to BF16 precision, where the row maximum and the
+    lazily moved reference decide everything.  Within the BF16 gate.  (Logits of 2^24 and
+    beyond are outside the kernel's range: see the fused exponent argument.)"""
+    S, H = 300, 2
+    inp = make_inputs(small_case(1, H, S, 71))
+    gain = torch.pow(2.0, torch.tensor([0.0, 4.0, 7.0, 10.0]).repeat_interleave(75)).view(1, S, 1, 1)
+    inp.q = (inp.q.double() * gain).to(torch.bfloat16)
+    g = to_device(inp, cuda_dev)
+    o = sa.attn_fwd_bf16(g.q, g.k, g.v)
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    check(o, inp.q, inp.k, inp.v, 1 / math.sqrt(128), "logits up to ~2000")

@@ -20,9 +20,9 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from parity import (BF16_A, BF16_B, SAGE_A, SAGE_B, assert_sage_exact_gate, assert_sage_format_gate,
-                    gather_rows, metrics)
-from workloads import make_inputs, sample_rows, small_case, to_device
+from parity import (BF16_A, BF16_B, SAGE_A, SAGE_B, assert_bf16_gate, assert_sage_exact_gate,
+                    assert_sage_format_gate, gather_rows, metrics)
+from workloads import make_inputs, sample_rows, small_case, to_device, wide_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -188,3 +188,27 @@ def test_key_value_reversal_permutes_the_format(cuda_dev, pv):
     d = metrics(gather_rows(o2, rows), gather_rows(o1, rows), a_abs_v, 2 * a, 2 * b)
     print(pv, "reversed vs forward:", d)
     assert d["bound_ratio"] <= 1.0 and d["cos"] >= 0.999, d
+
+
+def test_saturated_softmax_large_scores(cuda_dev):
+    """Q blocks up to 2^13 next to ordinary and subnormal ones: block scales up to ~60 and
+    scores up to ~5e5 (log2 units), a one-hot softmax, next to blocks whose scores are
+    ~1e-38.  Both Sage modes within their format gates.  (Scores of 2^24 and beyond are
+    outside the kernel's range: see the fused exponent argument.)"""
+    S, H = 256, 2
+    ranges = [(-20, 13), (5, 13), (-3, 3), (8, 13), (0, 1), (-60, 13), (10, 13), (-130, -123)]
+    inp = make_inputs(small_case(1, H, S, 1820))
+    inp.q = torch.cat([wide_bf16(1830 + i, (1, 32, H, 128), lo, hi) for i, (lo, hi) in enumerate(ranges)], dim=1)
+    g = to_device(inp, cuda_dev)
+    o8 = sa.sage_attention(g.q, g.k, g.v)
+    o16 = sa.sage_attention(g.q, g.k, g.v, pv="bf16")
+    torch.cuda.synchronize()
+    sa.attn_get_device_status()
+    rows = oracle.all_rows(1, S, H)
+    prep = oracle.prepare(inp.q, inp.k, inp.v, 1 / math.sqrt(128))
+    m8 = metrics(gather_rows(o8, rows), oracle.sage_attention(prep, S, rows, H),
+                 oracle.sage_attention(prep, S, rows, H, abs_v=True), SAGE_A, SAGE_B)
+    assert_sage_format_gate(m8, "e4m3 P, scores up to 5e5")
+    m16 = metrics(gather_rows(o16, rows), oracle.sage_attention_v16(prep, inp.v, rows),
+                  oracle.sage_attention_v16(prep, inp.v, rows, abs_v=True), BF16_A, BF16_B)
+    assert_bf16_gate(m16, "BF16 P, scores up to 5e5")

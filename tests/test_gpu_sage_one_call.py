@@ -105,9 +105,7 @@ def test_q_coded_on_load_extreme_blocks(cuda_dev):
     overflows (every code +-127: the forward's clamped branch) and subnormal ones,
     next to blocks spanning many binades."""
     S, H = 256, 2
-    # the largest blocks stay below 2^13, which keeps every score below 2^20 in magnitude (both
-    # kernels form 2^(t - m) with a fused multiply-add, whose residual against the rounded
-    # maximum only stays negligible while |t| is well below 2^24)
+    # scores stay below 2^20 (beyond 2^24 they are outside the kernels' range)
     ranges = [(-130, -123), (-20, 13), (5, 13), (-133, -126), (-3, 3), (-126, -100), (0, 1), (-60, 13)]
     q = torch.cat([wide_bf16(1800 + i, (1, 32, H, 128), lo, hi) for i, (lo, hi) in enumerate(ranges)], dim=1)
     inp = make_inputs(small_case(1, H, S, 1810))
