@@ -117,6 +117,7 @@ struct __align__(1024) Smem {
   uint64_t o_done[kNQ];
   uint64_t mma_drain;
   uint64_t q_ready[kNQ];     // quantise-on-load: all 128 rows of Q_i coded in place
+  float v_scale[128];        // FP8 mode: the head's V channel scales, for the epilogue
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -285,6 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
+  }
+  if constexpr (kMode == Mode::kSageFP8) {
+    // staged once: every epilogue thread reads all 128, which from global memory would cost
+    // a round of load latency per 32-column chunk at the end of every CTA
+    if (threadIdx.x < 128) sm.v_scale[threadIdx.x] = __ldg(p.v_scale + (long long)bh * 128 + threadIdx.x);
   }
   tc_fence_before();
   __syncthreads();
@@ -680,7 +686,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n > 0 && mbar_wait_warp<true>(&sm.o_done[i], (n - 1) & 1, abort_flag, err, kErrTimeoutMma)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float* vs = kFP8 ? p.v_scale + (long long)bh * 128 : nullptr;
       const int b = bh / p.H, h = bh % p.H;
       __nv_bfloat16* dst = p.o + (long long)b * p.o_sb + (long long)grow * p.o_ss + (long long)h * p.o_sh;
 #pragma unroll
@@ -693,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           if constexpr (kFP8) {
-            const float2 sv = __ldg(reinterpret_cast<const float2*>(vs + 32 * cc + 2 * e));
+            const float2 sv = *reinterpret_cast<const float2*>(&sm.v_scale[32 * cc + 2 * e]);
             w[e] = pack_bf16x2(u2f(o[2 * e]) * (sv.x * inv_l), u2f(o[2 * e + 1]) * (sv.y * inv_l));
           } else {
             w[e] = pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l);
