@@ -323,6 +323,14 @@ def run_ours(args, rank, world):
         "e2e": e2e,
     }
     result["clocks"] = clk.summary()
+    # the secondary bound of either attention path: one exp2 per score, B*H*S^2 of them, at
+    # the MUFU rate measured on this part (30 results per clock per SM, f32 or packed f16x2)
+    exps = wl.B * wl.H * wl.S * wl.S
+    sm_hz = (result["clocks"].get("sm_mhz") or 2070.0) * 1e6
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    result["exp_bound"] = {"exps": exps, "results_per_clk_per_sm": 30, "sm_mhz": sm_hz / 1e6,
+                           "floor_ms": exps / (30 * n_sms * sm_hz) * 1e3,
+                           "frac_of_bf16_step_time": exps / (30 * n_sms * sm_hz) * 1e3 / step_ms["bf16"]}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     return result
@@ -426,8 +434,18 @@ def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
     t0 = time.perf_counter()
     oracle.attention(q, k, v, wl.softmax_scale, rows=rows)
     dt = time.perf_counter() - t0
-    return {"value": n * per_row / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s"}
+    out = {"value": n * per_row / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s"}
+    # and the whole tiny workload (B=1 H=2 S=512) on one thread
+    from workloads import WORKLOADS
+    tw = WORKLOADS["tiny"]
+    ti = make_inputs(tw)
+    t0 = time.perf_counter()
+    oracle.attention(ti.q, ti.k, ti.v, tw.softmax_scale, nthreads=1)
+    dt1 = time.perf_counter() - t0
+    out["single_thread_tiny"] = {"value": roofline.attention_flops(tw.B, tw.H, tw.S, tw.D) / dt1 / 1e12,
+                                 "unit": "TFLOPS", "seconds": dt1, "sample": "all rows of tiny, 1 thread"}
+    return out
 
 
 def run_reference(args, rank, world):
