@@ -93,9 +93,10 @@ struct CfgBF16V {
   static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   static constexpr int kVTileBytes = 128 * 128 * 2;
-  // BF16 keeps FP32's exponent range, so the reference may lag far: p <= 2^32 stays
-  // exact to BF16 precision and the FP32 sums cannot overflow, and O is rescaled rarely
-  static constexpr float kTau = 32.0f;
+  // BF16 keeps FP32's exponent range, so the reference may lag far and O is rescaled
+  // rarely: p <= 2^64 keeps BF16 precision, and the FP32 sums of O stay finite while
+  // |V| * S < 2^64 (~1.8e19)
+  static constexpr float kTau = 64.0f;
 };
 template <>
 struct Cfg<Mode::kSagePV16> : CfgBF16V {};
