@@ -123,6 +123,17 @@ void oracle_f32_to_bf16_array(const float* x, uint16_t* out, int64_t n) {
 
 /* ------------------------------------------------------------- attention */
 
+/* Threads for one call: nthreads if > 0, else all.  Passed as the parallel region's
+ * num_threads clause, so a call never changes the count later calls see. */
+static int oracle_team_size(int nthreads) {
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
 /*
  * O[b, s, h, :] = sum_j w_j V[b, j, h, :] / sum_j w_j,
  *   w_j = exp(t_j - max_j t_j),  t_j = scale * <Q[b, s, h, :], K[b, j, h, :]>,
@@ -136,11 +147,9 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       int B, int S, int H, int D, double scale,
                       const int64_t* rows, int64_t n_rows, double* out, int nthreads) {
     int64_t total = rows ? n_rows : (int64_t)B * S * H;
-    (void)nthreads;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
-#pragma omp parallel
+    const int nt = oracle_team_size(nthreads);
+    (void)nt;
+#pragma omp parallel num_threads(nt)
     {
         double* t = (double*)malloc(sizeof(double) * (size_t)S);
         double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -429,12 +438,10 @@ void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8
                            int64_t n_rows, int abs_v, int p_e4m3, double* out, int nthreads) {
     int64_t nblk = S_pad / 32;
     (void)B;
-    (void)nthreads;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
+    const int nt = oracle_team_size(nthreads);
+    (void)nt;
     e4m3_init();
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
     {
         double* t = (double*)malloc(sizeof(double) * (size_t)S);
         double acc[128];
@@ -486,11 +493,9 @@ void oracle_sage_attention_v16(const int8_t* q8, const int8_t* k8, const float* 
                                int64_t n_rows, int abs_v, double* out, int nthreads) {
     int64_t nblk = S_pad / 32;
     (void)B;
-    (void)nthreads;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#endif
-#pragma omp parallel
+    const int nt = oracle_team_size(nthreads);
+    (void)nt;
+#pragma omp parallel num_threads(nt)
     {
         double* t = (double*)malloc(sizeof(double) * (size_t)S);
         double acc[128];
