@@ -435,7 +435,9 @@ def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
     oracle.attention(q, k, v, wl.softmax_scale, rows=rows)
     dt = time.perf_counter() - t0
     out = {"value": n * per_row / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-           "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s"}
+           "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s",
+           # the whole workload's rows at the sampled rate (not measured: extrapolated)
+           "extrapolated_full_s": dt * (wl.B * wl.S * wl.H) / n}
     # and the whole tiny workload (B=1 H=2 S=512) on one thread
     from workloads import WORKLOADS
     tw = WORKLOADS["tiny"]

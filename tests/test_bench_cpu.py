@@ -11,6 +11,7 @@ def test_cpu_baseline_keys_and_thread_count():
     r = bench.cpu_baseline(WORKLOADS["tiny"], seconds=0.3)
     assert r["kind"] == "oracle" and r["unit"] == "TFLOPS" and r["value"] > 0
     assert r["cores"] == before and "query rows of tiny" in r["sample"]
+    assert r["extrapolated_full_s"] > 0
     st = r["single_thread_tiny"]
     assert st["value"] > 0 and st["seconds"] > 0 and st["sample"] == "all rows of tiny, 1 thread"
     assert oracle.num_threads() == before
