@@ -1,7 +1,8 @@
-"""The library's own linkage (the DiT flash-kernel note's and RDNAttention's
-point that the kernels are self-contained, no vendor attention or BLAS): the
-built libsageattn.so needs the CUDA runtime and the C/C++ system libraries and
-nothing else -- no cuBLAS, cuDNN or other kernel library.  The TMA descriptor
+"""The library's own linkage, the check the RDNA2 DiT flash-kernel note reports
+(Results and Reproducibility / Provenance: dynamic linkage to the base runtime and
+system libraries only, no vendor BLAS or attention library): the built
+libsageattn.so needs the CUDA runtime and the C/C++ system libraries and nothing
+else -- no cuBLAS, cuDNN or other kernel library.  The TMA descriptor
 encoder is reached through the runtime's driver entry point, so libcuda is not
 linked either.  Reads the dynamic section with readelf; no GPU involved."""
 import re
