@@ -47,3 +47,27 @@ def test_ties_go_to_even():
     y = t + MAGIC
     n = y.view(np.int32).astype(np.int64) - 0x4B400000
     assert n.tolist() == [0, 2, 2, 0, -2, 126, -126]
+
+
+def test_int8_to_fp16_widening_is_exact():
+    # the two-call path's widening: byte u = code + 128 as the FP16 pattern 0x6400 | u is
+    # 1024 + u, and 1024 + u - 1152 is the code -- for all 256 codes, in FP16 arithmetic
+    codes = np.arange(-128, 128, dtype=np.int64)
+    u = (codes + 128).astype(np.uint16)
+    h = (np.uint16(0x6400) | u).view(np.float16)
+    assert np.array_equal(h.astype(np.float64), 1024.0 + u)
+    widened = (h - np.float16(1152)).astype(np.float64)       # one FP16 subtraction, exact
+    assert np.array_equal(widened, codes.astype(np.float64))
+
+
+def test_int8_score_products_accumulate_exactly_in_fp32():
+    # Q K^T on the FP16 codes with an FP32 accumulator: every product (<= 127^2) and every
+    # partial sum over the 128 channels (<= 128 * 127^2 < 2^24) is an integer binary32 holds
+    assert 128 * 127 * 127 < 2 ** 24
+    rng = np.random.default_rng(5)
+    q = rng.integers(-127, 128, size=(64, 128)).astype(np.float32)
+    k = rng.integers(-127, 128, size=(64, 128)).astype(np.float32)
+    acc = np.zeros((64, 64), dtype=np.float32)
+    for c in range(128):                                       # sequential binary32 accumulation
+        acc = acc + np.outer(q[:, c], k[:, c]).astype(np.float32)
+    assert np.array_equal(acc.astype(np.int64), q.astype(np.int64) @ k.astype(np.int64).T)
