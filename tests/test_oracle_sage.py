@@ -3,6 +3,7 @@ import math
 import os
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -94,3 +95,22 @@ def test_key_value_reversal_permutes_codes_and_keeps_the_format_value():
     oa = oracle.sage_attention(a, S, rows, H)
     ob = oracle.sage_attention(b, S, rows, H)
     assert np.abs(oa - ob).max() <= 1e-12
+
+
+@pytest.mark.parametrize("S,kw", [(1000, {}), (2000, dict(outlier_frac=0.05, outlier_gain=8.0)),
+                                  (700, dict(k_channel_offset_std=2.0))])
+def test_format_gate_covers_e4m3_rounding_of_p(S, kw):
+    """The Sage kernel's gate against the exact format value, 1e-3 + (2^-4 + 2^-8) A|V|,
+    is derived from rounding every probability to e4m3 (relative error <= 2^-4) with the
+    denominator left unrounded.  The oracle's own e4m3-P evaluation must therefore sit
+    inside it, outlier-dominated rows included, and well inside for the cosine."""
+    from parity import SAGE_A, SAGE_B, metrics
+    inp = make_inputs(small_case(1, 2, S, 520 + S, **kw))
+    sm = 1 / math.sqrt(128)
+    prep = oracle.prepare(inp.q, inp.k, inp.v, sm)
+    rows = oracle.all_rows(1, S, 2)[::5]
+    exact = oracle.sage_attention(prep, S, rows, 2)
+    abs_v = oracle.sage_attention(prep, S, rows, 2, abs_v=True)
+    rounded = oracle.sage_attention(prep, S, rows, 2, p_e4m3=True)
+    m = metrics(rounded, exact, abs_v, SAGE_A, SAGE_B)
+    assert m["bound_ratio"] <= 1.0 and m["cos"] >= 0.999, m
