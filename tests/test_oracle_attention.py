@@ -184,3 +184,32 @@ def test_planted_scale_mistake_is_caught():
     wrong = oracle.attention(q, k, v, 1.0)
     right = sdpa64(q, k, v, 1 / math.sqrt(128))
     assert np.abs(wrong - right).max() > 1e-3
+
+
+def _bf16(x):
+    """float64 -> nearest BF16 value, through binary32 as the kernel's conversions do."""
+    x32 = np.asarray(x, dtype=np.float32)
+    return (oracle.f32_to_bf16(x32).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("S,kw", [(1000, {}), (2000, dict(outlier_frac=0.05, outlier_gain=8.0))])
+def test_bf16_gate_covers_the_bf16_roundings(S, kw):
+    """The BF16 path's gate, 2e-2 + 2^-7 A|V| with cosine >= 0.99999, is derived from what
+    the kernel rounds: every probability to BF16 for the P V product (the denominator from
+    the unrounded ones) and O once to BF16.  Emulated in FP64 on plain and outlier-dominated
+    rows, that rounding stays inside the gate."""
+    from parity import BF16_A, BF16_B, metrics
+    inp = make_inputs(small_case(1, 2, S, 540 + S, **kw))
+    sm = 1 / math.sqrt(128)
+    rows = oracle.all_rows(1, S, 2)[::7]
+    exact = oracle.attention(inp.q, inp.k, inp.v, sm, rows=rows)
+    q, k, v = (x.double().numpy() for x in (inp.q, inp.k, inp.v))
+    got = np.empty_like(exact)
+    av = np.empty_like(exact)
+    for n, (b, s, h) in enumerate(rows.tolist()):
+        t = (k[b, :, h] @ q[b, s, h]) * sm
+        w = np.exp(t - t.max())
+        got[n] = _bf16((_bf16(w) @ v[b, :, h]) / w.sum())
+        av[n] = (w @ np.abs(v[b, :, h])) / w.sum()
+    m = metrics(got, exact, av, BF16_A, BF16_B)
+    assert m["bound_ratio"] <= 1.0 and m["cos"] >= 0.99999, m
