@@ -272,3 +272,19 @@ def test_flop_model_reproduces_handbook_block_profile():
     assert f"{flops / 1e9:.1f}" == g["gflop"]
     assert f"{byts / 2 ** 20:.0f}" == g["mbytes"]
     assert f"{flops / byts:.0f}" == g["intensity"]
+
+
+@pytest.mark.parametrize("name,gb", [("flux2048", 1.14), ("wan720p", 4.29), ("hunyuan720p", 4.03)])
+def test_prepare_byte_model_matches_the_scope_figures(name, gb):
+    """The prepare's algorithmic bytes (the benchmark's HBM-fraction numerator): read Q, K, V
+    and V again, write the INT8 Q/K and e4m3 V codes and the scales (plus the RoPE tables and
+    RMSNorm weights where fused) -- 1.14, 4.29 and 4.03 GB at the FLUX-2048, Wan-720p and
+    HunyuanVideo-720p shapes, and K smoothing adds one more pass over K and its block sums."""
+    from workloads import WORKLOADS
+    w = WORKLOADS[name]
+    S_pad = oracle.padded_len(w.S)
+    got = roofline.prepare_bytes(w.B, w.H, w.S, S_pad, 128, w.rms_norm, w.rope_dim)
+    assert abs(got / 1e9 - gb) < 0.01
+    bsh = w.B * w.S * w.H * 128
+    smooth = roofline.prepare_smooth_k_bytes(w.B, w.H, w.S, S_pad, 128, w.rms_norm, w.rope_dim)
+    assert smooth - got == bsh * 2 + 2 * w.B * w.H * (S_pad // 32) * 128 * 4 + 2 * w.B * w.H * 128 * 4
