@@ -10,7 +10,11 @@ Tolerances, from the arithmetic of each path:
   once more (<= 2^-8 |O| <= 2^-8 A|V|); 2e-2 is the absolute tolerance the
   acceptance criteria state for everything else.  On rows dominated by a few
   x8 outlier tokens A|V| reaches ~30, where no BF16 kernel that rounds P can
-  stay within an absolute 2e-2.
+  stay within an absolute 2e-2.  Where no such rows exist (N(0,1) inputs: the
+  tiny, FLUX-1024, FLUX-2048 and HunyuanVideo workloads and the small cases)
+  the stated bound itself, max |O - O_ref| <= 2e-2, is asserted as well
+  (assert_bf16_raw); only the Wan-720p workload, with its x8 outlier tokens,
+  relies on the derived bound alone.
   Sage path vs the exact value of its own format (FP64 attention on the
   prepared INT8 / e4m3 codes): cosine >= 0.999 and
       |O - O_fmt| <= 1e-3 + (2^-4 + 2^-8) * A|V|_fmt
@@ -47,6 +51,12 @@ def assert_bf16_gate(m: dict, what: str = ""):
     assert not m["nan"], f"{what}: NaN in output {m}"
     assert m["cos"] >= 0.99999, f"{what}: cosine {m}"
     assert m["bound_ratio"] <= 1.0, f"{what}: error above 2e-2 + 2^-7 A|V| {m}"
+
+
+def assert_bf16_raw(m: dict, what: str = ""):
+    """The BF16 path's stated acceptance bound, max-abs <= 2e-2 against FP64, for inputs
+    without outlier-dominated rows."""
+    assert m["max_abs"] <= 2e-2, f"{what}: raw max-abs above 2e-2 {m}"
 
 
 def assert_sage_format_gate(m: dict, what: str = ""):

@@ -4,7 +4,8 @@ Small and ragged shapes are compared on every element; the DiT-shaped
 workloads on sampled rows (every row of the ragged last tile, outlier tokens
 where the workload has them, the rest uniform), run in the launch
 configuration the benchmark times.  Gate: cosine >= 0.99999 and
-|O - O_ref| <= 2e-2 + 2^-7 A|V| elementwise (derivation in tests/parity.py).
+|O - O_ref| <= 2e-2 + 2^-7 A|V| elementwise (derivation in tests/parity.py);
+on inputs without x8 outlier tokens also the stated max-abs <= 2e-2 itself.
 """
 import math
 
@@ -14,7 +15,7 @@ import torch
 
 import oracle
 import sage_attention_forward_gb300 as sa
-from parity import BF16_A, BF16_B, assert_bf16_gate, gather_rows, metrics
+from parity import BF16_A, BF16_B, assert_bf16_gate, assert_bf16_raw, gather_rows, metrics
 from workloads import make_inputs, sample_rows, small_case, to_device, wide_bf16, WORKLOADS
 
 pytestmark = pytest.mark.gpu
@@ -25,11 +26,14 @@ def reference(q, k, v, scale, rows=None):
     return (oracle.attention(q, k, v, scale, rows=rows), oracle.attention(q, k, v.abs(), scale, rows=rows))
 
 
-def check(o, q, k, v, scale, what, rows=None):
+def check(o, q, k, v, scale, what, rows=None, raw=True):
+    """raw: also assert max-abs <= 2e-2 (inputs without outlier-dominated rows)."""
     ref, av = reference(q, k, v, scale, rows)
     m = metrics(o if rows is None else gather_rows(o, rows), ref, av, BF16_A, BF16_B)
     print(what, m)
     assert_bf16_gate(m, what)
+    if raw:
+        assert_bf16_raw(m, what)
     return m
 
 
@@ -64,7 +68,9 @@ def test_dit_workloads_sampled_rows(cuda_dev, workload_inputs, name, n_rows):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     rows = sample_rows(cpu.wl, n_rows, outlier_tokens=cpu.outlier_tokens)
-    check(o, cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, name, rows=rows)
+    # the Wan-720p workload's x8 outlier rows put the stated 2e-2 out of reach of any
+    # kernel that rounds P to BF16 (tests/parity.py): there the derived bound alone
+    check(o, cpu.q, cpu.k, cpu.v, cpu.wl.softmax_scale, name, rows=rows, raw=not cpu.wl.outlier_frac)
 
 
 def test_permuted_output_layout(cuda_dev, workload_inputs):
@@ -111,7 +117,9 @@ def test_other_softmax_scale(cuda_dev):
     g = to_device(inp, cuda_dev)
     for scale in (0.02, 0.3):
         o = sa.attn_fwd_bf16(g.q, g.k, g.v, softmax_scale=scale)
-        check(o, inp.q, inp.k, inp.v, scale, f"scale {scale}")
+        # at scale 0.3 a row's weight sits on a few keys, |O| approaches max |V| and the
+        # BF16 spacing of the output alone is up to 2^-6: the derived bound there
+        check(o, inp.q, inp.k, inp.v, scale, f"scale {scale}", raw=scale < 0.1)
 
 
 def test_device_status_is_clean(cuda_dev):
@@ -131,4 +139,4 @@ def test_saturated_softmax_large_logits(cuda_dev):
     o = sa.attn_fwd_bf16(g.q, g.k, g.v)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
-    check(o, inp.q, inp.k, inp.v, 1 / math.sqrt(128), "logits up to ~2000")
+    check(o, inp.q, inp.k, inp.v, 1 / math.sqrt(128), "logits up to ~2000", raw=False)

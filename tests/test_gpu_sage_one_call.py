@@ -5,16 +5,23 @@ workspace the forward reads and V's as sage_prepare does, and the forward's
 arithmetic from the codes on is the same.  With q_on_load the forward codes Q
 itself as it loads it (RMSNorm and RoPE first when asked); equal outputs then
 pin those in-kernel Q codes and scales to the prepare's, which
-test_gpu_prepare.py pins to the oracle bit for bit.  (The two-call path is checked against the oracle
-in test_gpu_prepare.py, test_gpu_sage.py, test_gpu_sage_pv16.py and
-test_gpu_smooth_k.py.)"""
+test_gpu_prepare.py pins to the oracle bit for bit.  Every output with Q coded
+on load is also compared with the oracle directly, on the same shapes: with
+the format gate against the exact value of its format (oracle.sage_attention
+for e4m3 P V, oracle.sage_attention_v16 for the 16-bit P V) and with the
+acceptance gates against the FP64 attention of the BF16 inputs (after the
+oracle's RMSNorm + RoPE), as test_gpu_sage.py and test_gpu_sage_pv16.py do for
+the two-call path."""
 import dataclasses
 
 import pytest
 import torch
 
+import oracle
 import sage_attention_forward_gb300 as sa
-from workloads import make_inputs, small_case, to_device, wide_bf16
+from parity import (BF16_A, BF16_B, SAGE_A, SAGE_B, assert_bf16_gate, assert_sage_exact_gate,
+                    assert_sage_format_gate, gather_rows, metrics)
+from workloads import make_inputs, sample_rows, small_case, to_device, wide_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +42,38 @@ def two_calls(g, wl, smooth_k, pv):
     return sa.sage_attn_fwd(prep)
 
 
+def oracle_check(o, cpu, pv, smooth_k=False, rows=None, exact_gate=True):
+    """The output against the oracle: the format gate against its format's exact value
+    and the acceptance gates against FP64 attention of the (normed, roped) BF16 inputs
+    (exact_gate False: within 0.002 of the format's own cosine there instead; None: the
+    format gate alone)."""
+    wl = cpu.wl
+    if rows is None:
+        rows = oracle.all_rows(wl.B, wl.S, wl.H)
+    prep = oracle.prepare(cpu.q, cpu.k, cpu.v, wl.softmax_scale, q_norm_w=cpu.q_norm_w, k_norm_w=cpu.k_norm_w,
+                          rms_eps=wl.rms_eps, rope_cos=cpu.rope_cos, rope_sin=cpu.rope_sin, rope_dim=wl.rope_dim,
+                          smooth_k=smooth_k)
+    got = gather_rows(o, rows)
+    if pv == "bf16":
+        fmt = oracle.sage_attention_v16(prep, cpu.v, rows)
+        m_fmt = metrics(got, fmt, oracle.sage_attention_v16(prep, cpu.v, rows, abs_v=True), BF16_A, BF16_B)
+        assert_bf16_gate(m_fmt, "q_on_load, 16-bit P V, vs format")
+    else:
+        fmt = oracle.sage_attention(prep, wl.S, rows, wl.H)
+        m_fmt = metrics(got, fmt, oracle.sage_attention(prep, wl.S, rows, wl.H, abs_v=True), SAGE_A, SAGE_B)
+        assert_sage_format_gate(m_fmt, "q_on_load, e4m3 P V, vs format")
+    if exact_gate is None:
+        return
+    exact = oracle.attention(prep["q_pre"], prep["k_pre"], cpu.v, wl.softmax_scale, rows=rows)
+    m_exact = metrics(got, exact)
+    print("q_on_load", pv, "vs format:", m_fmt, "\n   vs exact:", m_exact)
+    if exact_gate:
+        assert_sage_exact_gate(m_exact, f"q_on_load {pv} vs exact")
+    else:
+        m_floor = metrics(fmt, exact)
+        assert m_exact["cos"] >= m_floor["cos"] - 0.002, f"{m_exact} vs format floor {m_floor}"
+
+
 @pytest.mark.parametrize("q_on_load", [False, True])
 @pytest.mark.parametrize("pv", ["e4m3", "bf16"])
 @pytest.mark.parametrize("smooth_k", [False, True])
@@ -49,6 +88,8 @@ def test_one_call_equals_two_calls(cuda_dev, B, H, S, kw, smooth_k, pv, q_on_loa
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     assert torch.equal(o1, o2)
+    if q_on_load:
+        oracle_check(o1, inp, pv, smooth_k)
 
 
 @pytest.mark.parametrize("pv", ["e4m3", "bf16"])
@@ -84,6 +125,7 @@ def test_q_coded_on_load_with_norm_and_rope(cuda_dev, rope_dim, norm, pv):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     assert torch.equal(o1, o2)
+    oracle_check(o1, inp, pv)
 
 
 @pytest.mark.parametrize("S", [129, 300, 513])
@@ -98,6 +140,7 @@ def test_q_coded_on_load_zero_eps_ragged(cuda_dev, S):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     assert torch.equal(o1, o2)
+    oracle_check(o1, inp, "e4m3")
 
 
 def test_q_coded_on_load_extreme_blocks(cuda_dev):
@@ -117,6 +160,9 @@ def test_q_coded_on_load_extreme_blocks(cuda_dev):
         torch.cuda.synchronize()
         sa.attn_get_device_status()
         assert torch.equal(o1, o2), pv
+        # one-hot softmaxes next to blocks whose scores are ~1e-38: the format gate, as the
+        # two-call path's saturated-softmax test asks
+        oracle_check(o1, inp, pv, exact_gate=None)
 
 
 @pytest.mark.parametrize("name", ["flux2048", "hunyuan720p"])
@@ -129,3 +175,4 @@ def test_q_coded_on_load_workloads(cuda_dev, workload_inputs, name):
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     assert torch.equal(o1, o2)
+    oracle_check(o1, cpu, "e4m3", rows=sample_rows(cpu.wl, 384, outlier_tokens=cpu.outlier_tokens))
