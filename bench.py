@@ -151,6 +151,55 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- ours
+class SmClock:
+    """Average SM clock over a stretch of the stream, from the library's SM clock sampler
+    (every SM's %clock64 against %globaltimer): sample() before and after, mhz() once
+    both have completed.  The samples are enqueued outside the event-timed spans."""
+
+    def __init__(self, sa, torch, dev, n_sms):
+        self.sa, self.torch, self.dev, self.n = sa, torch, dev, max(n_sms, 1) + 32
+
+    def sample(self, stream):
+        buf = self.torch.empty((self.n, 2), dtype=self.torch.int64, device=self.dev)
+        return self.sa.sm_clock_sample(buf, stream=stream)
+
+    def mhz(self, a, b):
+        return self.sa.sm_clock_mhz(a.cpu().numpy(), b.cpu().numpy())
+
+
+def time_providers(calls, stream, clk, rounds=3, warm=2, reps=5):
+    """Each provider alone: `warm` warm-up calls, then `reps` calls between two events
+    (and two SM clock samples), `rounds` rounds with the providers interleaved.
+    Returns name -> {"ms": median per-call ms, "sm_mhz": median clock, "mcycles": median
+    per-call SM cycles / 1e6}."""
+    import torch
+    got = {name: [] for name in calls}
+    for _ in range(rounds):
+        for name, fn in calls.items():
+            for _ in range(warm):
+                fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            c0 = clk.sample(stream)
+            ev[0].record(stream)
+            for _ in range(reps):
+                fn()
+            ev[1].record(stream)
+            c1 = clk.sample(stream)
+            ev[1].synchronize()
+            torch.cuda.synchronize()
+            ms = ev[0].elapsed_time(ev[1]) / reps
+            mhz = clk.mhz(c0, c1)
+            got[name].append((ms, mhz, ms * mhz / 1e3 if mhz else None))
+    out = {}
+    for name, t in got.items():
+        cyc = [c for _, _, c in t if c is not None]
+        mh = [m for _, m, _ in t if m is not None]
+        out[name] = {"ms": statistics.median([m for m, _, _ in t]),
+                     "sm_mhz": statistics.median(mh) if mh else None,
+                     "mcycles": statistics.median(cyc) if cyc else None}
+    return out
+
+
 def run_ours(args, rank, world):
     import torch
     import sage_attention_forward_gb300 as sa
@@ -159,6 +208,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     wl = WORKLOADS[args.workload]
     B, H, S, D = wl.B, wl.H, wl.S, wl.D
     inp = make_inputs(wl, device=dev)          # drawn on the device: inputs resident in HBM
@@ -171,12 +221,9 @@ def run_ours(args, rank, world):
     ws_p = sa.prepare_workspace(B, H, dev)
     ws_a = sa.attn_workspace(B, H, S_pad, dev)
     ws_1 = sa.sage_attention_workspace(B, H, S, dev)
-    kw = {}
-    if inp.q_norm_w is not None:
-        kw.update(q_norm_w=inp.q_norm_w, k_norm_w=inp.k_norm_w, rms_eps=wl.rms_eps)
-    if inp.rope_cos is not None:
-        kw.update(rope_cos=inp.rope_cos, rope_sin=inp.rope_sin, rope_dim=wl.rope_dim)
+    kw = norm_rope_kwargs(inp, wl)
     stream = torch.cuda.current_stream()
+    clk = SmClock(sa, torch, dev, n_sms)
 
     def step(ev=None):
         if ev is not None:
@@ -205,15 +252,18 @@ def run_ours(args, rank, world):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index) as smi:
         barrier()
+        c_start = clk.sample(stream)
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         t_end.record(stream)
+        c_end = clk.sample(stream)
         barrier()
     sa.attn_get_device_status()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    region_mhz = clk.mhz(c_start, c_end)
 
     # the step's own split (each call timed inside the interleaved step)
     per = {"bf16": [], "sage": []}
@@ -224,9 +274,34 @@ def run_ours(args, rank, world):
     step_ms = {k2: statistics.mean(v2) for k2, v2 in per.items()}
     peaks = load_peaks()
 
+    # the same split with each call's own SM clock (clock samples between the calls of a
+    # few more steps, outside the timed region): cycles take the power cap's clock out
+    split = {"bf16": [], "sage": []}
+    for _ in range(3):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        c0 = clk.sample(stream)
+        ev[0].record(stream)
+        sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale)
+        ev[1].record(stream)
+        c1 = clk.sample(stream)
+        ev[2].record(stream)
+        sa.sage_attention(q, k, v, softmax_scale=scale, out=o_sage, workspace=ws_1, **kw)
+        ev[3].record(stream)
+        c2 = clk.sample(stream)
+        torch.cuda.synchronize()
+        for name, a, b, e0, e1 in (("bf16", c0, c1, ev[0], ev[1]), ("sage", c1, c2, ev[2], ev[3])):
+            ms = e0.elapsed_time(e1)
+            mhz = clk.mhz(a, b)
+            split[name].append((ms, mhz, ms * mhz / 1e3 if mhz else None))
+    in_step = {name: {"ms": statistics.median([t[0] for t in v2]),
+                      "sm_mhz": statistics.median([t[1] for t in v2 if t[1]]) if any(t[1] for t in v2) else None,
+                      "mcycles": statistics.median([t[2] for t in v2 if t[2]]) if any(t[2] for t in v2) else None}
+               for name, v2 in split.items()}
+
     # providers, each timed on its own: 2 warm-up + 5 back-to-back calls, 3 rounds with the
     # providers interleaved, median.  Inside the step the GPU's power management carries
-    # clock headroom from one kernel into the next, which skews a per-call split.
+    # clock headroom from one kernel into the next, which skews a per-call split; the
+    # cycle counts (time x the call's own average SM clock) do not depend on it.
     o_pv16 = torch.empty_like(o_bf16)
     prep_s = sa.Prepared.empty(B, H, S, S_pad, dev)
     ws_s = sa.prepare_workspace(B, H, dev, S_pad, smooth_k=True)
@@ -250,54 +325,86 @@ def run_ours(args, rank, world):
         "prepare_smooth_k": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep_s,
                                                     workspace=ws_s, smooth_k=True, **kw),
     }
-    rounds = {name: [] for name in calls}
-    for _ in range(3):
-        for name, fn in calls.items():
-            for _ in range(2):
-                fn()
-            ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            ev_p[0].record(stream)
-            for _ in range(5):
-                fn()
-            ev_p[1].record(stream)
-            ev_p[1].synchronize()
-            rounds[name].append(ev_p[0].elapsed_time(ev_p[1]) / 5)
+    timed = time_providers(calls, stream, clk)
     sa.attn_get_device_status()
-    ms = {name: statistics.median(t) for name, t in rounds.items()}
     prep_bytes = roofline.prepare_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
     smooth_bytes = roofline.prepare_smooth_k_bytes(B, H, S, S_pad, D, wl.rms_norm, wl.rope_dim)
+    rate_bf16 = roofline.TC_FLOP_PER_CLK_SM["f16"]
+    rate_sage = roofline.sage_flop_per_clk_sm()
 
-    def tf(name):
-        return F / (ms[name] * 1e-3) / 1e12
+    def attn_entry(name, rate=None, call=None):
+        t = timed[name]
+        e = {"ms": t["ms"], "tflops": F / (t["ms"] * 1e-3) / 1e12, "sm_mhz": t["sm_mhz"], "mcycles": t["mcycles"]}
+        if rate is not None and t["sm_mhz"]:
+            e["frac_of_clock_peak"] = e["tflops"] / roofline.clock_peak_tflops(rate, n_sms, t["sm_mhz"])
+        if call:
+            e["call"] = call
+        return e
 
-    bf16_tflops = tf("bf16")
-    # the roofline's kernel time is its average launch inside the timed region
-    roof_tflops = F / (step_ms["bf16"] * 1e-3) / 1e12
+    def hbm_entry(name, nbytes):
+        t = timed[name]
+        gbs = nbytes / (t["ms"] * 1e-3) / 1e9
+        return {"ms": t["ms"], "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm"], "sm_mhz": t["sm_mhz"]}
+
     providers = {
-        "bf16": {"ms": ms["bf16"], "tflops": bf16_tflops},
-        "sage": {"ms": ms["sage"], "tflops": tf("sage"), "call": "sage_attention (prepare + forward, one call)"},
-        "sage_two_calls": {"ms": ms["sage_two_calls"], "tflops": tf("sage_two_calls"),
-                           "call": "sage_prepare, then sage_attn_fwd"},
-        "sage_pv16": {"ms": ms["sage_pv16"], "tflops": tf("sage_pv16"), "call": "sage_attention(pv=bf16)"},
-        "sage_q_on_load": {"ms": ms["sage_q_on_load"], "tflops": tf("sage_q_on_load"),
-                           "call": "sage_attention(q_on_load=True): Q coded by the forward"},
-        "sage_core": {"ms": ms["sage_core"], "tflops": tf("sage_core"),
-                      # QK^T on the FP16 MMA (BF16 rate), PV on the e4m3 MMA (twice that rate)
-                      "frac_of_tensor_roof": tf("sage_core") / (peaks["bf16_sustained"] / 0.75)},
-        "sage_pv16_core": {"ms": ms["sage_pv16_core"], "tflops": tf("sage_pv16_core"),
-                           "frac_of_tensor_roof": tf("sage_pv16_core") / peaks["bf16_sustained"]},
-        "prepare": {"ms": ms["prepare"], "gbs": prep_bytes / (ms["prepare"] * 1e-3) / 1e9,
-                    "frac_of_hbm": prep_bytes / (ms["prepare"] * 1e-3) / 1e9 / peaks["hbm"]},
-        "prepare_smooth_k": {"ms": ms["prepare_smooth_k"],
-                             "gbs": smooth_bytes / (ms["prepare_smooth_k"] * 1e-3) / 1e9,
-                             "frac_of_hbm": smooth_bytes / (ms["prepare_smooth_k"] * 1e-3) / 1e9 / peaks["hbm"]},
-        "timing": "each provider alone: 2 warm-up + 5 calls, 3 interleaved rounds, median",
+        "bf16": attn_entry("bf16", rate_bf16),
+        "sage": attn_entry("sage", None, "sage_attention (prepare + forward, one call)"),
+        "sage_two_calls": attn_entry("sage_two_calls", None, "sage_prepare, then sage_attn_fwd"),
+        "sage_pv16": attn_entry("sage_pv16", None, "sage_attention(pv=bf16)"),
+        "sage_q_on_load": attn_entry("sage_q_on_load", None, "sage_attention(q_on_load=True): Q coded by the forward"),
+        # Q K^T on the FP16 MMA (the kind::f16 rate), P V on the e4m3 MMA (twice that rate)
+        "sage_core": attn_entry("sage_core", rate_sage),
+        "sage_pv16_core": attn_entry("sage_pv16_core", rate_bf16),
+        "prepare": hbm_entry("prepare", prep_bytes),
+        "prepare_smooth_k": hbm_entry("prepare_smooth_k", smooth_bytes),
+        "timing": "each provider alone: 2 warm-up + 5 calls, 3 interleaved rounds, median; sm_mhz: the call's own "
+                  "average SM clock (SM cycle counters against the GPU timer), mcycles = ms x sm_mhz / 1e3",
         "in_step_ms": step_ms,
+        "in_step": in_step,
+    }
+    providers["sage_vs_bf16"] = {
+        "alone_time_ratio": timed["sage"]["ms"] / timed["bf16"]["ms"],
+        "alone_cycle_ratio": (timed["sage"]["mcycles"] / timed["bf16"]["mcycles"]
+                              if timed["sage"]["mcycles"] and timed["bf16"]["mcycles"] else None),
+        "in_step_time_ratio": in_step["sage"]["ms"] / in_step["bf16"]["ms"],
+        "in_step_cycle_ratio": (in_step["sage"]["mcycles"] / in_step["bf16"]["mcycles"]
+                                if in_step["sage"]["mcycles"] and in_step["bf16"]["mcycles"] else None),
+        "note": "one-call Sage (prepare included) over BF16; below 1 means Sage is faster",
     }
     del prep_s, ws_s, o_pv16, ws_16, ws_ql
 
     # ------------------------------------------------------------- end to end
     e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)
+
+    # the roofline of the dominant kernel: the BF16 forward's average launch inside the
+    # timed step, against the measured sustained BF16 peak and against the per-clock
+    # tcgen05 rate at the SM clock averaged over the timed region
+    roof_tflops = F / (step_ms["bf16"] * 1e-3) / 1e12
+    roof = {"bound": "tensor", "kernel": "attn_fwd_bf16 (average launch inside the timed step)",
+            "achieved": roof_tflops, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+            "frac": roof_tflops / peaks["bf16_sustained"],
+            "traffic": kernel_traffic("attn_fwd_bf16", wl.name),
+            "peak_source": f"{peaks['source']} bf16 sustained (of {peaks['source']})"}
+    if region_mhz:
+        cp = roofline.clock_peak_tflops(rate_bf16, n_sms, region_mhz)
+        roof.update({"sm_mhz": region_mhz, "clock_peak": cp, "frac_of_clock_peak": roof_tflops / cp,
+                     "clock_peak_source": f"tcgen05 kind::f16 {rate_bf16:.0f} FLOP/clk/SM (probe) x {n_sms} SMs x "
+                                          "the SM clock averaged over the timed region"})
+    # the Sage forward alone: half the FLOPs at the FP16 rate, half at the e4m3 rate; the
+    # measured BF16 burst peak / 0.75 is that mix at the measured rate
+    sc = timed["sage_core"]
+    sage_tflops = F / (sc["ms"] * 1e-3) / 1e12
+    roof_sage = {"bound": "tensor", "kernel": "attn_fwd_kernel Sage FP8 mode (sage_core, timed alone)",
+                 "achieved": sage_tflops, "peak": peaks["bf16"] / 0.75, "unit": "TFLOP/s",
+                 "frac": sage_tflops / (peaks["bf16"] / 0.75),
+                 "traffic": kernel_traffic("attn_fwd_sage_fp8", wl.name),
+                 "peak_source": f"{peaks['source']} bf16 burst / 0.75 (half the FLOPs at the e4m3 rate, twice the "
+                                f"BF16 rate; no INT8 tensor-core MMA on sm_103a)"}
+    if sc["sm_mhz"]:
+        cp = roofline.clock_peak_tflops(rate_sage, n_sms, sc["sm_mhz"])
+        roof_sage.update({"sm_mhz": sc["sm_mhz"], "clock_peak": cp, "frac_of_clock_peak": sage_tflops / cp,
+                          "clock_peak_source": f"{rate_sage:.0f} FLOP/clk/SM (harmonic mean of the probe's kind::f16 "
+                                               f"and e4m3 rates) x {n_sms} SMs x the call's SM clock"})
 
     result = {
         "metric": METRIC,
@@ -314,26 +421,84 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": workload_config(wl, world),
         "providers": providers,
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_bf16", "achieved": roof_tflops,
-                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": roof_tflops / peaks["bf16_sustained"],
-                     "traffic": kernel_traffic("attn_fwd_bf16", wl.name),
-                     "peak_source": f"{peaks['source']} bf16 sustained"},
+        "roofline": roof,
+        "roofline_sage": roof_sage,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": e2e,
     }
-    result["clocks"] = clk.summary()
+    result["clocks"] = smi.summary()
+    result["clocks"]["sm_mhz_probe"] = region_mhz
     # the secondary bound of either attention path: one exp2 per score, B*H*S^2 of them, at
     # the MUFU rate measured on this part (30 results per clock per SM, f32 or packed f16x2)
     exps = wl.B * wl.H * wl.S * wl.S
-    sm_hz = (result["clocks"].get("sm_mhz") or 2070.0) * 1e6
-    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_hz = (region_mhz or result["clocks"].get("sm_mhz") or 2070.0) * 1e6
     result["exp_bound"] = {"exps": exps, "results_per_clk_per_sm": 30, "sm_mhz": sm_hz / 1e6,
                            "floor_ms": exps / (30 * n_sms * sm_hz) * 1e3,
                            "frac_of_bf16_step_time": exps / (30 * n_sms * sm_hz) * 1e3 / step_ms["bf16"]}
+    if not args.no_per_workload:
+        del prep, ws_p, ws_a, ws_1, o_bf16, o_sage, inp, q, k, v
+        torch.cuda.empty_cache()
+        result["per_workload"] = per_workload(sa, roofline, torch, dev, stream, clk, n_sms, wl.name)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     return result
+
+
+def norm_rope_kwargs(inp, wl):
+    kw = {}
+    if inp.q_norm_w is not None:
+        kw.update(q_norm_w=inp.q_norm_w, k_norm_w=inp.k_norm_w, rms_eps=wl.rms_eps)
+    if inp.rope_cos is not None:
+        kw.update(rope_cos=inp.rope_cos, rope_sin=inp.rope_sin, rope_dim=wl.rope_dim)
+    return kw
+
+
+PER_WORKLOADS = ("flux1024", "flux2048", "hunyuan720p")
+
+
+def per_workload(sa, roofline, torch, dev, stream, clk, n_sms, skip):
+    """The pages' other DiT shapes (the handbook's byte table): BF16 forward, one-call Sage
+    (with the fused RMSNorm + RoPE where the workload has it) and the Sage forward alone,
+    each timed on its own, with SM clocks and clock-normalised roof fractions."""
+    from workloads import WORKLOADS, make_inputs
+    out = {}
+    for name in PER_WORKLOADS:
+        if name == skip:
+            continue
+        wl = WORKLOADS[name]
+        B, H, S, D = wl.B, wl.H, wl.S, wl.D
+        inp = make_inputs(wl, device=dev)
+        kw = norm_rope_kwargs(inp, wl)
+        S_pad = sa.sage_padded_len(S)
+        o1 = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+        o2 = torch.empty_like(o1)
+        ws_1 = sa.sage_attention_workspace(B, H, S, dev)
+        prep = sa.sage_prepare(inp.q, inp.k, inp.v, softmax_scale=wl.softmax_scale, **kw)
+        ws_a = sa.attn_workspace(B, H, S_pad, dev)
+        calls = {
+            "bf16": lambda: sa.attn_fwd_bf16(inp.q, inp.k, inp.v, out=o1, softmax_scale=wl.softmax_scale),
+            "sage": lambda: sa.sage_attention(inp.q, inp.k, inp.v, softmax_scale=wl.softmax_scale, out=o2,
+                                              workspace=ws_1, **kw),
+            "sage_core": lambda: sa.sage_attn_fwd(prep, out=o2, workspace=ws_a),
+        }
+        t = time_providers(calls, stream, clk)
+        sa.attn_get_device_status()
+        F = roofline.attention_flops(B, H, S, D)
+        entry = {"config": f"B={B} H={H} S={S} D={D}" + (f", RMSNorm + RoPE {wl.rope_dim} fused" if kw else "")
+                           + (", head-major [B,H,S,D] storage" if wl.head_major_storage else "")}
+        for prov, rate in (("bf16", roofline.TC_FLOP_PER_CLK_SM["f16"]), ("sage", None),
+                           ("sage_core", roofline.sage_flop_per_clk_sm())):
+            e = {"ms": t[prov]["ms"], "tflops": F / (t[prov]["ms"] * 1e-3) / 1e12, "sm_mhz": t[prov]["sm_mhz"],
+                 "mcycles": t[prov]["mcycles"]}
+            if rate is not None and t[prov]["sm_mhz"]:
+                e["frac_of_clock_peak"] = e["tflops"] / roofline.clock_peak_tflops(rate, n_sms, t[prov]["sm_mhz"])
+            entry[prov] = e
+        entry["sage_vs_bf16_cycle_ratio"] = (t["sage"]["mcycles"] / t["bf16"]["mcycles"]
+                                             if t["sage"]["mcycles"] and t["bf16"]["mcycles"] else None)
+        out[name] = entry
+        del inp, o1, o2, ws_1, prep, ws_a, calls
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
@@ -415,9 +580,11 @@ def _oracle_rows(wl, n, seed):
     return sample_rows(wl, n, seed=seed, must_include_tail=False)
 
 
-def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
+def cpu_baseline(wl, seconds: float = 15.0, inputs=None, full_workloads=("tiny", "flux1024"), flux2048_rows=2048):
     """Time the oracle's FP64 attention on sampled query rows of the workload
-    (every row a full softmax over all S keys), on all host cores."""
+    (every row a full softmax over all S keys), on all host cores; then the whole
+    tiny and FLUX-1024 workloads (every row, all cores) and a bounded row sample of
+    FLUX-2048, whose full run (about 7e12 FP64 FLOP) takes minutes."""
     import oracle
     from workloads import make_inputs
     from sage_attention_forward_gb300 import roofline
@@ -438,8 +605,8 @@ def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
            "sample": f"{n} query rows of {wl.name} (each a full FP64 softmax over S={wl.S} keys), {dt:.1f} s",
            # the whole workload's rows at the sampled rate (not measured: extrapolated)
            "extrapolated_full_s": dt * (wl.B * wl.S * wl.H) / n}
-    # and the whole tiny workload (B=1 H=2 S=512) on one thread
     from workloads import WORKLOADS
+    # the whole tiny workload (B=1 H=2 S=512) on one thread
     tw = WORKLOADS["tiny"]
     ti = make_inputs(tw)
     t0 = time.perf_counter()
@@ -447,6 +614,29 @@ def cpu_baseline(wl, seconds: float = 15.0, inputs=None):
     dt1 = time.perf_counter() - t0
     out["single_thread_tiny"] = {"value": roofline.attention_flops(tw.B, tw.H, tw.S, tw.D) / dt1 / 1e12,
                                  "unit": "TFLOPS", "seconds": dt1, "sample": "all rows of tiny, 1 thread"}
+    # full tensors where the oracle finishes in seconds, all host cores
+    full = {}
+    for name in full_workloads:
+        fw = WORKLOADS[name]
+        fi = ti if name == "tiny" else make_inputs(fw)
+        t0 = time.perf_counter()
+        oracle.attention(fi.q, fi.k, fi.v, fw.softmax_scale)
+        dtf = time.perf_counter() - t0
+        full[name] = {"value": roofline.attention_flops(fw.B, fw.H, fw.S, fw.D) / dtf / 1e12, "unit": "TFLOPS",
+                      "seconds": dtf, "cores": oracle.num_threads(),
+                      "sample": f"every row of {name} (B={fw.B} H={fw.H} S={fw.S}), measured"}
+    # FLUX-2048: a bounded row sample, extrapolated to the full tensor and labelled so
+    fw = WORKLOADS["flux2048"]
+    fi = make_inputs(fw)
+    n2 = flux2048_rows
+    t0 = time.perf_counter()
+    oracle.attention(fi.q, fi.k, fi.v, fw.softmax_scale, rows=_oracle_rows(fw, n2, 3))
+    dt2 = time.perf_counter() - t0
+    full["flux2048"] = {"value": n2 * 4 * fw.S * fw.D / dt2 / 1e12, "unit": "TFLOPS", "seconds": dt2,
+                        "cores": oracle.num_threads(),
+                        "sample": f"{n2} query rows of flux2048 (each over all S={fw.S} keys), measured",
+                        "extrapolated_full_s": dt2 * (fw.B * fw.S * fw.H) / n2}
+    out["per_workload"] = full
     return out
 
 
@@ -488,6 +678,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
     args = ap.parse_args()
 
     rank, world, local_rank = rank_info()

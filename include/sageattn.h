@@ -32,6 +32,7 @@
  * quantisation) and sage_attn_fwd_pv16 (P V in 16 bits with V unquantised),
  * both from the handbook's SageAttention section; sage_prepare_noalloc (no
  * workspace argument); attn_selftest_wait_timeout (exercises the failure path);
+ * attn_sm_clock_sample (SM clock counters, for timing);
  * sizes and status helpers.
  *
  * Conventions shared by every call
@@ -59,6 +60,13 @@
  *     word; attn_get_device_status() reports and clears it.
  *   - The library runs on sm_103 devices only; elsewhere every call returns
  *     ATTN_ERR_UNSUPPORTED.
+ *   - Sizes: B * H * S_pad / 128 must stay below 2^31 (S_pad = the padded
+ *     length, sage_padded_len(S) where the call takes none); the prepare
+ *     stages also take at most 65535 heads per batch entry (H <= 65535).
+ *     Larger calls return ATTN_ERR_INVALID_ARG.
+ *   - Host-side state (the device check, kernel attributes, the SM count) is
+ *     set up on first use in each CUDA context, under a lock: calls may come
+ *     from several host threads.
  */
 #ifndef SAGEATTN_H_
 #define SAGEATTN_H_
@@ -203,8 +211,11 @@ ATTN_API attn_status sage_prepare_smooth_k(const void* q, const void* k, const v
  *   - the array lives on every device that loads the library, until the process
  *     exits; this function never calls cudaMalloc, cudaFree or any allocating
  *     routine;
- *   - its first call on a device looks the array's device address up (a driver
- *     query, once per device); make that first call before capturing a stream;
+ *   - its first call in a CUDA context looks the array's device address up
+ *     (a runtime query, once per context: the address belongs to the module as
+ *     loaded in that context, so a reset device or a second context of the
+ *     same device looks it up again); make that first call before capturing
+ *     a stream;
  *   - all calls on a device share the array: the call clears it on `stream`
  *     before use, so what an earlier call left does not matter, but two calls
  *     whose work can overlap on the GPU (different streams without ordering)
@@ -336,6 +347,20 @@ ATTN_API attn_status attn_get_device_status(attn_stream_t stream);
  */
 ATTN_API attn_status attn_selftest_wait_timeout(const void* q, const void* k, const void* v, void* o,
                                                 attn_stream_t stream);
+
+/*
+ * attn_sm_clock_sample -- an instrumentation helper for timing, not part of the
+ * method: enqueues on `stream` a clear of `out` and a small kernel whose CTAs
+ * record, for the SM each runs on, that SM's cycle counter (%clock64) and the
+ * GPU's nanosecond timer (%globaltimer).  Two samples around a region give each
+ * SM's average clock over it: (cycles_b - cycles_a) / (ns_b - ns_a) GHz.
+ *   out     : device uint64 [n_slots][2] = {cycles, ns} per SM index (%smid);
+ *             slots of SMs that ran no CTA stay 0
+ *   n_slots : >= the device's SM count (SM indices past it are not recorded)
+ * Errors: NULL or misaligned out, n_slots < 1 -> ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_ALIGNMENT; launch failure -> ATTN_ERR_CUDA.
+ */
+ATTN_API attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_stream_t stream);
 
 /* attn_last_error -- message of the calling thread's last failed call ("" if none). */
 ATTN_API const char* attn_last_error(void);

@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.sage_attention.restype = i
         L.attn_selftest_wait_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.attn_selftest_wait_timeout.restype = i
+        L.attn_sm_clock_sample.argtypes = [_vp, i, _vp]
+        L.attn_sm_clock_sample.restype = i
         L.attn_get_device_status.argtypes = [_vp]
         L.attn_get_device_status.restype = i
         L.attn_last_error.argtypes = []
@@ -162,6 +164,28 @@ class Prepared:
                         torch.empty((B, H, 128), dtype=torch.float32, device=device), S, S_pad)
 
 
+def _check_prepared(out: Prepared, q: torch.Tensor, S_pad: int | None = None) -> None:
+    """A caller-supplied Prepared must match q's batch, heads and length: the kernels write
+    through its pointers with the sizes these imply."""
+    B, S, H, _ = q.shape
+    S_pad = out.S_pad if S_pad is None else S_pad
+    if out.S != S or out.S_pad != S_pad:
+        raise AttnError(1, f"out was made for S={out.S}, S_pad={out.S_pad}; this call has S={S}, S_pad={S_pad}")
+    want = {"q_i8": ((B, H, S_pad, 128), torch.int8), "k_i8": ((B, H, S_pad, 128), torch.int8),
+            "v_fp8": ((B, H, 128, S_pad), torch.uint8), "q_scale": ((B, H, S_pad // 32), torch.float32),
+            "k_scale": ((B, H, S_pad // 32), torch.float32), "v_scale": ((B, H, 128), torch.float32)}
+    if out.k_mean is not None:
+        want["k_mean"] = ((B, H, 128), torch.float32)
+    for name, (shape, dtype) in want.items():
+        t = getattr(out, name)
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise AttnError(1, f"out.{name} is {tuple(t.shape)} {t.dtype}, expected {shape} {dtype}")
+        if t.device != q.device:
+            raise AttnError(1, f"out.{name} is on {t.device}, q on {q.device}")
+        if not t.is_contiguous():
+            raise AttnError(1, f"out.{name} must be contiguous")
+
+
 def prepare_workspace(B: int, H: int, device, S_pad: int | None = None, smooth_k: bool = False) -> torch.Tensor:
     if smooth_k:
         n = int(lib().sage_prepare_smooth_k_workspace_size(B, H, int(S_pad)))
@@ -189,6 +213,9 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
         S_pad = sage_padded_len(S)
     if out is None:
         out = Prepared.empty(B, H, S, S_pad, q.device)
+    if smooth_k and out.k_mean is None:
+        out.k_mean = torch.empty((B, H, 128), dtype=torch.float32, device=q.device)
+    _check_prepared(out, q, S_pad)
     if workspace is None:
         workspace = prepare_workspace(B, H, q.device, S_pad, smooth_k)
     qs, ks, vs = _bshd("q", q), _bshd("k", k), _bshd("v", v)
@@ -197,8 +224,6 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
         return None if t is None else t.data_ptr()
 
     if smooth_k:
-        if out.k_mean is None:
-            out.k_mean = torch.empty((B, H, 128), dtype=torch.float32, device=q.device)
         _check(lib().sage_prepare_smooth_k(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                                            float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps),
                                            ptr(rope_cos), ptr(rope_sin), int(rope_dim), int(S_pad),
@@ -232,6 +257,7 @@ def sage_prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out:
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     qs, ks, vs = _bshd("q", q), _bshd("k", k), _bshd("v", v)
+    _check_prepared(out, q)
 
     def ptr(t):
         return None if t is None else t.data_ptr()
@@ -324,6 +350,28 @@ def attn_selftest_wait_timeout(device=None, stream=None) -> str:
     bufs = [torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev) for _ in range(4)]
     code = lib().attn_selftest_wait_timeout(*(b.data_ptr() for b in bufs), _stream_ptr(stream))
     return STATUS.get(code, str(code))
+
+
+def sm_clock_sample(out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Enqueue a sample of every SM's cycle counter and the GPU's nanosecond timer into
+    out (int64 [n_slots, 2] on the device, n_slots >= the SM count): timing
+    instrumentation, see attn_sm_clock_sample in include/sageattn.h."""
+    if out.dtype != torch.int64 or out.dim() != 2 or out.shape[1] != 2 or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA int64 tensor [n_slots, 2]")
+    _check(lib().attn_sm_clock_sample(out.data_ptr(), out.shape[0], _stream_ptr(stream)))
+    return out
+
+
+def sm_clock_mhz(a, b) -> float | None:
+    """Median over SMs of the average SM clock (MHz) between two host copies of
+    sm_clock_sample outputs; None if no SM appears in both."""
+    import numpy as np
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    ok = (a[:, 0] > 0) & (b[:, 0] > 0) & (b[:, 1] > a[:, 1])
+    if not ok.any():
+        return None
+    return float(np.median((b[ok, 0] - a[ok, 0]) / (b[ok, 1] - a[ok, 1]) * 1e3))
 
 
 def attn_get_device_status(stream=None) -> None:

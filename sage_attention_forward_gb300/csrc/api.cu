@@ -120,6 +120,14 @@ attn_status tmap_bytes_3d(CUtensorMap* m, const void* ptr, long long n0, long lo
 // ------------------------------------------------------------------ validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The kernels run one CTA per (head, 128 padded positions) at most, numbered along
+// grid.x: B * H * S_pad / 128 must stay below 2^31.
+attn_status check_grid(int B, int H, long long S_pad) {
+  if ((long long)B * H * (S_pad / 128) > 0x7fffffffLL)
+    return fail(ATTN_ERR_INVALID_ARG, "B=%d H=%d S_pad=%lld: B*H*S_pad/128 must be below 2^31", B, H, S_pad);
+  return ATTN_OK;
+}
+
 // B = 0 or H = 0 (no query rows at all) is a valid empty problem: *empty is set and the
 // caller returns ATTN_OK without touching its pointers.  S = 0 is an error: attention over
 // no keys is undefined.
@@ -132,9 +140,7 @@ attn_status check_shape(int B, int S, int H, int D, bool* empty) {
     *empty = true;
     return ATTN_OK;
   }
-  if (B > 65535 || H > 65535 || (long long)B * H > 65535)
-    return fail(ATTN_ERR_INVALID_ARG, "B=%d H=%d: B*H must be <= 65535", B, H);
-  return ATTN_OK;
+  return check_grid(B, H, ((long long)S + 127) / 128 * 128);
 }
 
 // Strides of a [B, S, H, 128] tensor; a dimension of extent 1 gets a harmless
@@ -161,16 +167,52 @@ attn_status check_strides(const char* name, const void* ptr, const int64_t* in, 
 }  // namespace
 
 namespace sa {
-int device_sm_count() {
-  static int cache[kMaxDevices] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+namespace {
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+}  // namespace
+
+cudaError_t current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {
+    // nothing current on this thread yet: make the current device's primary context
+    // current, as the runtime's next call would
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
   }
-  return cache[dev];
+  if (g_ctx_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+int device_sm_count() {
+  static PerContext<int> cache;
+  int n = 0;
+  cudaError_t e = cache.get([](int* v) {
+    int dev = 0, m = 0;
+    cudaError_t r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess && m <= 0) r = cudaErrorInvalidValue;
+    *v = m;
+    return r;
+  }, &n);
+  return e == cudaSuccess ? n : 148;
 }
 }  // namespace sa
 
@@ -210,80 +252,6 @@ attn_status attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, 
   return ATTN_OK;
 }
 
-attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, int B, int S, int H, int D,
-                                 const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
-                                 float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
-                                 const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
-                                 int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
-                                 float* v_scale, attn_stream_t stream) {
-  bool empty = false;
-  TRY(check_shape(B, S, H, D, &empty));
-  if (empty) return ATTN_OK;
-  if ((long long)B * H > sa::kNoAllocMaxHeads)
-    return fail(ATTN_ERR_INVALID_ARG,
-                "sage_prepare_noalloc: B*H=%lld heads exceeds the %d heads its static scratch holds; use "
-                "sage_prepare with a caller-allocated workspace",
-                (long long)B * H, sa::kNoAllocMaxHeads);
-  sa::PrepareArgs a;
-  TRY(check_strides("q", q, q_str, B, S, H, a.str[0]));
-  TRY(check_strides("k", k, k_str, B, S, H, a.str[1]));
-  TRY(check_strides("v", v, v_str, B, S, H, a.str[2]));
-  if (!std::isfinite(softmax_scale)) return fail(ATTN_ERR_INVALID_ARG, "softmax_scale is not finite");
-  if (S_pad < S || S_pad % 128 != 0)
-    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
-  if (S_pad / 32 > (1ll << 30)) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
-  if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
-    return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
-  if (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w)))
-    return fail(ATTN_ERR_ALIGNMENT, "RMSNorm weights must be 16-byte aligned");
-  if (q_norm_w && !(rms_eps >= 0.0f && std::isfinite(rms_eps)))
-    return fail(ATTN_ERR_INVALID_ARG, "rms_eps must be finite and >= 0");
-  if (!(rope_dim == 0 || rope_dim == 32 || rope_dim == 64 || rope_dim == 96 || rope_dim == 128))
-    return fail(ATTN_ERR_INVALID_ARG, "rope_dim=%d must be one of 0, 32, 64, 96, 128", rope_dim);
-  if (rope_dim > 0) {
-    if (!rope_cos || !rope_sin) return fail(ATTN_ERR_INVALID_ARG, "rope_dim > 0 needs rope_cos and rope_sin");
-    if (!aligned16(rope_cos) || !aligned16(rope_sin))
-      return fail(ATTN_ERR_ALIGNMENT, "RoPE tables must be 16-byte aligned");
-  }
-  struct {
-    const char* n;
-    const void* p;
-  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8},
-              {"q_scale", q_scale}, {"k_scale", k_scale}, {"v_scale", v_scale}};
-  for (auto& t : outs) {
-    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
-    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
-  }
-  TRY(check_device());
-  uint32_t* scratch = nullptr;
-  cudaError_t e = sa::noalloc_prepare_scratch(&scratch);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc: looking up the static scratch");
-  a.x[0] = q;
-  a.x[1] = k;
-  a.x[2] = v;
-  a.B = B;
-  a.S = S;
-  a.H = H;
-  a.S_pad = S_pad;
-  a.q_norm_w = q_norm_w;
-  a.k_norm_w = k_norm_w;
-  a.rms_eps = rms_eps;
-  a.rope_cos = rope_dim > 0 ? rope_cos : nullptr;
-  a.rope_sin = rope_dim > 0 ? rope_sin : nullptr;
-  a.rope_dim = rope_dim;
-  a.q_i8 = q_i8;
-  a.k_i8 = k_i8;
-  a.v_fp8 = v_fp8;
-  a.q_scale = q_scale;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  a.c_log2 = (float)((double)softmax_scale * kLog2e);
-  a.vmax = scratch;  // zeroed on the stream by the launcher before the kernels use it
-  e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc launch");
-  return ATTN_OK;
-}
-
 int64_t sage_padded_len(int64_t S) { return S <= 0 ? 0 : ((S + 127) / 128) * 128; }
 
 size_t sage_prepare_workspace_size(int B, int H) {
@@ -305,6 +273,8 @@ static attn_status prepare_inputs(const void* q, const void* k, const void* v, i
   if (S_pad < S || S_pad % 128 != 0)
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad / 32 > (1ll << 30)) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  TRY(check_grid(B, H, S_pad));
+  if (H > 65535) return fail(ATTN_ERR_INVALID_ARG, "H=%d: the prepare takes at most 65535 heads per batch entry", H);
   if ((q_norm_w == nullptr) != (k_norm_w == nullptr))
     return fail(ATTN_ERR_INVALID_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
   if (q_norm_w && (!aligned16(q_norm_w) || !aligned16(k_norm_w)))
@@ -335,6 +305,27 @@ static attn_status prepare_inputs(const void* q, const void* k, const void* v, i
   return ATTN_OK;
 }
 
+// The six prepare outputs: present and 16-byte aligned; then stored into `a`.
+static attn_status prepare_outputs(int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
+                                   float* v_scale, sa::PrepareArgs& a) {
+  struct {
+    const char* n;
+    const void* p;
+  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8},
+              {"q_scale", q_scale}, {"k_scale", k_scale}, {"v_scale", v_scale}};
+  for (auto& t : outs) {
+    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
+    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
+  }
+  a.q_i8 = q_i8;
+  a.k_i8 = k_i8;
+  a.v_fp8 = v_fp8;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return ATTN_OK;
+}
+
 static attn_status prepare_checked(const char* who, const void* q, const void* k, const void* v, int B, int S, int H, int D,
                          const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                          float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
@@ -348,25 +339,13 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
   sa::PrepareArgs a;
   TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
                      rope_sin, rope_dim, S_pad, a));
-  struct {
-    const char* n;
-    const void* p;
-  } outs[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale},
-              {"k_scale", k_scale}, {"v_scale", v_scale}, {"workspace", workspace}};
-  for (auto& t : outs) {
-    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
-    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
-  }
+  TRY(prepare_outputs(q_i8, k_i8, v_fp8, q_scale, k_scale, v_scale, a));
+  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   if (workspace_bytes < workspace_needed)
     return fail(ATTN_ERR_INVALID_ARG, "%s: workspace_bytes=%zu < %zu required", who, workspace_bytes,
                 workspace_needed);
   TRY(check_device());
-  a.q_i8 = q_i8;
-  a.k_i8 = k_i8;
-  a.v_fp8 = v_fp8;
-  a.q_scale = q_scale;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
   a.vmax = reinterpret_cast<uint32_t*>(workspace);
   if (k_mean != nullptr) {
     a.k_mean = k_mean;
@@ -388,6 +367,35 @@ attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int
                          k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8, q_scale,
                          k_scale, v_scale, workspace, workspace_bytes, sage_prepare_workspace_size(B, H), nullptr,
                          stream);
+}
+
+attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                 const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                 float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                 const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                 int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale,
+                                 float* v_scale, attn_stream_t stream) {
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
+  if ((long long)B * H > sa::kNoAllocMaxHeads)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "sage_prepare_noalloc: B*H=%lld heads exceeds the %d heads its static scratch holds; use "
+                "sage_prepare with a caller-allocated workspace",
+                (long long)B * H, sa::kNoAllocMaxHeads);
+  // the same validation as sage_prepare, short of the workspace
+  sa::PrepareArgs a;
+  TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
+                     rope_sin, rope_dim, S_pad, a));
+  TRY(prepare_outputs(q_i8, k_i8, v_fp8, q_scale, k_scale, v_scale, a));
+  TRY(check_device());
+  uint32_t* scratch = nullptr;
+  cudaError_t e = sa::noalloc_prepare_scratch(&scratch);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc: looking up the static scratch");
+  a.vmax = scratch;  // zeroed on the stream by the launcher before the kernels use it
+  e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_prepare_noalloc launch");
+  return ATTN_OK;
 }
 
 size_t sage_prepare_smooth_k_workspace_size(int B, int H, int64_t S_pad) {
@@ -429,6 +437,7 @@ attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t*
   if (S_pad < S || S_pad % 128 != 0)
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  TRY(check_grid(B, H, S_pad));
   struct {
     const char* n;
     const void* p;
@@ -471,6 +480,7 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
   if (S_pad < S || S_pad % 128 != 0)
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
+  TRY(check_grid(B, H, S_pad));
   struct {
     const char* n;
     const void* p;
@@ -659,6 +669,17 @@ attn_status attn_get_device_status(attn_stream_t stream) {
     return fail(ATTN_ERR_DEVICE_TIMEOUT,
                 "an attention kernel gave up on a bounded wait (bits 0x%x: 1 TMA load, 2 MMA commit, 4 hand-off; "
                 "0x100 a check build's TMEM-maximum mismatch)", w);
+  return ATTN_OK;
+}
+
+attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_stream_t stream) {
+  if (out == nullptr) return fail(ATTN_ERR_INVALID_ARG, "out is NULL");
+  if (!aligned16(out)) return fail(ATTN_ERR_ALIGNMENT, "out is not 16-byte aligned");
+  if (n_slots < 1) return fail(ATTN_ERR_INVALID_ARG, "n_slots=%d must be >= 1", n_slots);
+  TRY(check_device());
+  cudaError_t e = sa::launch_sm_clock_probe(reinterpret_cast<unsigned long long*>(out), n_slots,
+                                            sa::device_sm_count(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_sm_clock_sample launch");
   return ATTN_OK;
 }
 

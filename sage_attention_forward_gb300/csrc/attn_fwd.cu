@@ -136,6 +136,7 @@ struct Params {
   int H;
   int nblk;               // S_pad / 32
   int n_tiles;            // ceil(S / 128)
+  int BH;                 // B * H; the head of a CTA is blockIdx.y + gridDim.y * blockIdx.z
   int withhold_loads;     // self-test of the failure path: the producer loads nothing
   // quantise-on-load of Q
   const __nv_bfloat16* q_norm_w;   // [128] or nullptr
@@ -258,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem<kMode>& sm = *reinterpret_cast<Smem<kMode>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  // heads along grid.y and, beyond 65535 of them, grid.z (kept cheap to recompute from the
+  // special registers, so that it holds no register through the main loop)
+  const int bh = (int)(blockIdx.y + gridDim.y * blockIdx.z);
+  if (bh >= p.BH) return;   // the last grid.z slice may run past B * H
   const int q_row0 = blockIdx.x * (kNQ * kBM);
   const int n = p.n_tiles;
   volatile uint32_t* abort_flag = &sm.abort_flag;
@@ -761,16 +765,15 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
                           const float* q_scale, const float* k_scale, const float* v_scale, float c_log2, void* o,
                           long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
                           cudaStream_t stream, bool withhold_loads = false, const QLoadArgs* qa = nullptr) {
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  // the shared-memory opt-in is a property of the kernel in one CUDA context: set once per
+  // context (a reset device or another context of the same device needs it again)
+  static ContextOnce attr_done;
   const size_t smem = smem_bytes_of<kMode>();
-  if (!attr_done[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_kernel<kMode, kQLoad>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  cudaError_t e = attr_done.run([] {
+    return cudaFuncSetAttribute(attn_fwd_kernel<kMode, kQLoad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes_of<kMode>());
+  });
+  if (e != cudaSuccess) return e;
   Params p;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
@@ -784,6 +787,7 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   p.H = H;
   p.nblk = (int)(S_pad / 32);
   p.n_tiles = (S + kBN - 1) / kBN;
+  p.BH = B * H;
   p.withhold_loads = withhold_loads ? 1 : 0;
   p.q_norm_w = nullptr;
   p.rms_eps = 0.0f;
@@ -797,7 +801,10 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
     p.rope_dim = qa->rope_dim;
     p.c_log2 = qa->c_log2;
   }
-  dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), B * H, 1);
+  // Q blocks of one head are consecutive CTAs (they share that head's K/V in L2); heads go
+  // along grid.y, and grid.z when there are more than 65535 of them
+  const unsigned ny = (unsigned)(p.BH < 65535 ? p.BH : 65535);
+  dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), ny, (p.BH + ny - 1) / ny);
   attn_fwd_kernel<kMode, kQLoad><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
@@ -857,6 +864,29 @@ cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_
   // no prepared tensors: nblk = 1 is a placeholder, the scale pointers are not read
   return launch_kernel<Mode::kBF16>(tm_q, tm_k, tm_v, nullptr, nullptr, nullptr, c_log2, o, o_sb, o_ss, o_sh, B, S,
                                     H, 32, stream, withhold_loads);
+}
+
+namespace {
+// One thread per CTA records its SM's cycle counter and the global nanosecond timer.
+__global__ void __launch_bounds__(32) sm_clock_probe_kernel(unsigned long long* out, int n_slots) {
+  if (threadIdx.x != 0) return;
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  const unsigned long long c = clock64();
+  const unsigned long long t = globaltimer();
+  if (smid < (unsigned)n_slots) {
+    out[2 * smid] = c;
+    out[2 * smid + 1] = t;
+  }
+}
+}  // namespace
+
+cudaError_t launch_sm_clock_probe(unsigned long long* out, int n_slots, int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(out, 0, (size_t)n_slots * 2 * sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  // several CTAs per SM, so that every SM is very likely to run one
+  sm_clock_probe_kernel<<<4 * num_sms, 32, 0, stream>>>(out, n_slots);
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_err_attn(uint32_t* out) {

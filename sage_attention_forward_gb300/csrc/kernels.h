@@ -5,10 +5,69 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 namespace sa {
 
-// Number of SMs of the current device (cached per device).
+// The unique id (cuCtxGetId) of the CUDA context current on the calling thread; when none
+// is current yet, the current device's primary context is made current first, as the
+// runtime's next call would.  Ids are never reused within a process.
+cudaError_t current_context_id(unsigned long long* id);
+
+// A value made once per CUDA context and cached, thread-safe.  Keyed by the context id,
+// so a device that was reset, or a second context on the same device, makes its own
+// value; the cache keeps the last 64 contexts (an older one simply makes it again).
+template <class T>
+class PerContext {
+ public:
+  // make: cudaError_t(T*), called with the context current; its value is cached on success
+  template <class F>
+  cudaError_t get(F&& make, T* out) {
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu_);
+    for (int i = 0; i < kSlots && i < n_; ++i)
+      if (ids_[i] == id) {
+        *out = vals_[i];
+        return cudaSuccess;
+      }
+    T v{};
+    e = make(&v);
+    if (e != cudaSuccess) return e;
+    ids_[n_ % kSlots] = id;
+    vals_[n_ % kSlots] = v;
+    ++n_;
+    *out = v;
+    return cudaSuccess;
+  }
+
+ private:
+  static constexpr int kSlots = 64;
+  std::mutex mu_;
+  unsigned long long ids_[kSlots] = {};
+  T vals_[kSlots] = {};
+  int n_ = 0;
+};
+
+// A set-up step run once per CUDA context (e.g. a kernel attribute).
+class ContextOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& step) {
+    char done = 0;
+    return cache_.get([&](char* v) {
+      cudaError_t e = step();
+      *v = 1;
+      return e;
+    }, &done);
+  }
+
+ private:
+  PerContext<char> cache_;
+};
+
+// Number of SMs of the current device (cached per context).
 int device_sm_count();
 
 // The attention forward kernel, three modes (attn_fwd.cu).  BF16 flash attention:
@@ -17,6 +76,8 @@ int device_sm_count();
 cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                                  long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, float c_log2,
                                  cudaStream_t stream, bool withhold_loads = false);
+// Timing instrumentation: per-SM {clock64, globaltimer} into out[n_slots][2] (cleared first).
+cudaError_t launch_sm_clock_probe(unsigned long long* out, int n_slots, int num_sms, cudaStream_t stream);
 // The device error word all three modes record bounded-wait timeouts in.
 cudaError_t read_and_clear_err_attn(uint32_t* out);
 
@@ -49,8 +110,9 @@ struct PrepareArgs {
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 
-// Device address (current device) of the static scratch used by the
+// Device address, in the current context, of the static scratch used by the
 // allocation-free prepare entry point; it holds kNoAllocMaxHeads * 128 words.
+// Looked up on the first call in each context and cached.
 constexpr int kNoAllocMaxHeads = 2048;
 cudaError_t noalloc_prepare_scratch(uint32_t** out);
 

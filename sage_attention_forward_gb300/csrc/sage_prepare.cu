@@ -165,12 +165,19 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
 
 }
 
+// Grids of the per-block kernels: blockIdx.x = group of 8 blocks, blockIdx.y = head b * H + h
+// (at most 65535 heads per launch: the launcher splits larger batches).
+__device__ __forceinline__ void block_coords(int warp, int& bh, int& blk) {
+  bh = (int)blockIdx.y;
+  blk = (int)blockIdx.x * 8 + warp;
+}
+
 __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) {
   const int task = blockIdx.z + p.task0;
-  const int bh = blockIdx.y;
-  const int b = bh / p.H, h = bh % p.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x * 8 + warp;
+  int bh, blk;
+  block_coords(warp, bh, blk);
+  const int b = bh / p.H, h = bh % p.H;
   const int g = lane >> 3;   // row inside a 4-row step
   const int L = lane & 7;    // channel group [16L, 16L+16)
   const __nv_bfloat16* base = p.x[task] + (long long)b * p.sb[task] + (long long)h * p.sh[task] + 16 * L;
@@ -310,9 +317,9 @@ __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) 
 
 // One warp per (b, h, block), as the quantiser: block sums B_j into partial[bh][j][128].
 __global__ void __launch_bounds__(256) prep_kmean_partial_kernel(const QKParams p, float* __restrict__ partial) {
-  const int bh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x * 8 + warp;
+  int bh, blk;
+  block_coords(warp, bh, blk);
   if (blk >= p.nblk) return;
   const int g = lane >> 3;
   const int L = lane & 7;
@@ -374,19 +381,21 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
   o3 = __byte_perm(t1, t3, 0x7632);
 }
 
+// blockIdx.x = 128-position tile, blockIdx.y = head b * H + h
 __global__ void __launch_bounds__(128) prep_v_kernel(const VParams p) {
-  const int bh = blockIdx.y;
+  const int bh = (int)blockIdx.y;
+  const int tile = (int)blockIdx.x;
   const int b = bh / p.H, h = bh % p.H;
   const int c8 = threadIdx.x & 15;        // channels [8*c8, 8*c8 + 8)
   const int sg = threadIdx.x >> 4;        // positions [s0, s0 + 16)
-  const long long s0 = (long long)blockIdx.x * 128 + 16 * sg;
+  const long long s0 = (long long)tile * 128 + 16 * sg;
 
   float inv[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const float a = __uint_as_float(p.vmax[(long long)bh * 128 + 8 * c8 + k]);
     inv[k] = (a > 0.0f) ? __fdiv_rn(448.0f, a) : 0.0f;
-    if (blockIdx.x == 0 && sg == 0) p.scales[(long long)bh * 128 + 8 * c8 + k] = (a > 0.0f) ? __fdiv_rn(a, 448.0f) : 0.0f;
+    if (tile == 0 && sg == 0) p.scales[(long long)bh * 128 + 8 * c8 + k] = (a > 0.0f) ? __fdiv_rn(a, 448.0f) : 0.0f;
   }
 
   const __nv_bfloat16* base = p.v + (long long)b * p.sb + (long long)h * p.sh + 8 * c8;
@@ -427,26 +436,21 @@ __device__ __align__(256) static uint32_t g_prepare_scratch[kNoAllocMaxHeads * 1
 }  // namespace
 
 cudaError_t noalloc_prepare_scratch(uint32_t** out) {
-  // In host code g_prepare_scratch only names the symbol; its device address is
-  // looked up once per device, with that device current, and cached.
-  static std::mutex mu;
-  static uint32_t* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  // In host code g_prepare_scratch only names the symbol.  Its device address belongs to
+  // this library's module as loaded in one CUDA context, so it is looked up once per
+  // context, with that context current, and cached under the context's id.
+  static PerContext<uint32_t*> addr;
+  return addr.get([](uint32_t** v) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_prepare_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<uint32_t*>(p);
-  }
-  *out = addr[dev];
-  return cudaSuccess;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_prepare_scratch);
+    *v = static_cast<uint32_t*>(p);
+    return e;
+  }, out);
 }
 
-cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
+namespace {
+// One launch sequence for at most 65535 heads (B * H).
+cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   const int nblk = (int)(a.S_pad / 32);
   cudaError_t e = cudaSuccess;
   if (!a.skip_v) {
@@ -481,16 +485,19 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   p.vmax = a.vmax;
   p.kmean = a.k_mean;
   p.task0 = a.skip_q ? 1 : 0;
+  // heads along grid.y (at most 65535 per launch, which the caller below guarantees)
+  const int BH = a.B * a.H;
   if (a.k_mean != nullptr) {
-    dim3 g0((nblk + 7) / 8, a.B * a.H, 1);
+    dim3 g0((nblk + 7) / 8, BH, 1);
     prep_kmean_partial_kernel<<<g0, 256, 0, stream>>>(p, a.k_partial);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prep_kmean_kernel<<<a.B * a.H, 128, 0, stream>>>(a.k_partial, nblk, a.S, a.k_mean);
+    prep_kmean_kernel<<<BH, 128, 0, stream>>>(a.k_partial, nblk, a.S, a.k_mean);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 g1((nblk + 7) / 8, a.B * a.H, (a.skip_v ? 2 : 3) - p.task0);   // tasks [task0, 3 or 2)
+  // tasks [task0, 3 or 2) over grid.z
+  dim3 g1((nblk + 7) / 8, BH, (a.skip_v ? 2 : 3) - p.task0);
   prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -508,9 +515,43 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
   vp.vmax = a.vmax;
   vp.codes = a.v_fp8;
   vp.scales = a.v_scale;
-  dim3 g2((unsigned)(a.S_pad / 128), a.B * a.H, 1);
+  dim3 g2((unsigned)(a.S_pad / 128), BH, 1);
   prep_v_kernel<<<g2, 128, 0, stream>>>(vp);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
+  constexpr long long kMaxHeads = 65535;   // grid.y of the prepare kernels
+  if ((long long)a.B * a.H <= kMaxHeads) return launch_prepare_heads(a, stream);
+  if (a.H > kMaxHeads) return cudaErrorInvalidConfiguration;
+  // more heads than one grid holds: whole batch entries at a time, every pointer moved to
+  // the chunk's first batch entry (all per-head outputs are indexed by b * H + h)
+  const int per = (int)(kMaxHeads / a.H);
+  const long long S_pad = a.S_pad, nblk = S_pad / 32;
+  for (int b0 = 0; b0 < a.B; b0 += per) {
+    PrepareArgs c = a;
+    c.B = a.B - b0 < per ? a.B - b0 : per;
+    const long long h0 = (long long)b0 * a.H;   // first head of the chunk
+    for (int t = 0; t < 3; ++t)
+      c.x[t] = static_cast<const __nv_bfloat16*>(a.x[t]) + (long long)b0 * a.str[t][0];
+    auto bytes = [](void* p, long long off) { return p ? static_cast<void*>(static_cast<uint8_t*>(p) + off) : p; };
+    c.q_i8 = static_cast<int8_t*>(bytes(a.q_i8, h0 * S_pad * 128));
+    c.k_i8 = static_cast<int8_t*>(bytes(a.k_i8, h0 * S_pad * 128));
+    c.v_fp8 = static_cast<uint8_t*>(bytes(a.v_fp8, h0 * 128 * S_pad));
+    c.q16 = bytes(a.q16, h0 * S_pad * 128 * 2);
+    c.k16 = bytes(a.k16, h0 * S_pad * 128 * 2);
+    c.q_scale = static_cast<float*>(bytes(a.q_scale, h0 * nblk * 4));
+    c.k_scale = static_cast<float*>(bytes(a.k_scale, h0 * nblk * 4));
+    c.v_scale = static_cast<float*>(bytes(a.v_scale, h0 * 128 * 4));
+    c.vmax = static_cast<uint32_t*>(bytes(a.vmax, h0 * 128 * 4));
+    c.k_mean = static_cast<float*>(bytes(a.k_mean, h0 * 128 * 4));
+    c.k_partial = static_cast<float*>(bytes(a.k_partial, h0 * nblk * 128 * 4));
+    cudaError_t e = launch_prepare_heads(c, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace sa

@@ -69,3 +69,22 @@ def prepare_smooth_k_bytes(B: int, H: int, S: int, S_pad: int, D: int = 128, rms
     partials = 2 * B * H * (S_pad // 32) * D * 4
     means = 2 * B * H * D * 4
     return prepare_bytes(B, H, S, S_pad, D, rms_norm, rope_dim) + extra_k + partials + means
+
+
+# Dense tcgen05 MMA throughput per SM per clock on the GB300, measured by a probe
+# that issues back-to-back 128 x 128 (x 16 or x 32) MMAs from one thread and times
+# them with %clock64: kind::f16 (BF16 or FP16 operands, FP32 accumulator)
+# 8188 FLOP/clk/SM, kind::f8f6f4 with e4m3 operands 16376 FLOP/clk/SM.  The
+# clock-normalised roof of a kernel is this rate x SMs x its own average SM clock,
+# which takes the power-capped clock of a long run out of the fraction.
+TC_FLOP_PER_CLK_SM = {"f16": 8188.0, "e4m3": 16376.0}
+
+
+def sage_flop_per_clk_sm() -> float:
+    """The Sage forward's mixed rate: half of the FLOPs (Q K^T, INT8 codes widened to
+    FP16) at the kind::f16 rate, half (P V) at the e4m3 rate."""
+    return 2.0 / (1.0 / TC_FLOP_PER_CLK_SM["f16"] + 1.0 / TC_FLOP_PER_CLK_SM["e4m3"])
+
+
+def clock_peak_tflops(flop_per_clk_sm: float, n_sms: int, sm_mhz: float) -> float:
+    return flop_per_clk_sm * n_sms * sm_mhz * 1e6 / 1e12

@@ -57,7 +57,8 @@ def call_fwd(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, S=256, H=2, D=128, qs=(256 * 2
     (dict(qs=(256 * 2 * 128, 260, 128)), 2),
     (dict(qs=(256 * 2 * 128, -256, 128)), 1),
     (dict(scale=float("inf")), 1),
-    (dict(B=300, H=300), 1),
+    (dict(B=65536, H=16384), 1),       # B*H*S_pad/128 = 2^31 CTAs: beyond the grid
+    (dict(B=300, H=300, q=0), 1),      # 90000 heads are accepted (then the NULL q is reported)
 ])
 def test_attn_fwd_bf16_rejects_bad_arguments(kw, status):
     assert call_fwd(**kw) == status

@@ -7,7 +7,9 @@ mid-step, or they are plug-ins handed only their input and output buffers.
 This entry point takes no workspace: its scratch is a fixed array inside the
 library.  These tests check, through the C ABI, that it writes exactly what
 sage_prepare (which takes a caller-allocated workspace) writes, on two calls in
-a row with different shapes, and that calls beyond its fixed capacity are
+a row with different shapes, at its full capacity (2048 heads, the last slot
+of the fixed array in use) followed by a small call, and that calls beyond its
+fixed capacity, or with output buffers that do not match the inputs, are
 refused before anything is launched.  This file is collected last on purpose.
 """
 import ctypes
@@ -54,6 +56,37 @@ def test_matches_sage_prepare_on_two_calls_in_a_row(cuda_dev):
                 assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
             else:
                 assert torch.equal(a, b), name
+
+
+@pytest.mark.gpu
+def test_matches_sage_prepare_at_capacity(cuda_dev):
+    # B * H = 2048 heads fill the fixed scratch to its last slot; the ragged small call
+    # after it must see none of those channel maxima
+    for inp in (make_inputs(small_case(2, 1024, 40, 903)), make_inputs(small_case(1, 3, 77, 904))):
+        ref, out = _both(inp, cuda_dev)
+        for name in FIELDS:
+            a, b = getattr(ref, name), getattr(out, name)
+            if a.dtype == torch.float32:
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
+            else:
+                assert torch.equal(a, b), name
+
+
+@pytest.mark.gpu
+def test_refuses_outputs_made_for_other_shapes(cuda_dev):
+    # a Prepared made at set-up time for fewer heads or a shorter sequence would be written
+    # past its ends: the binding refuses it before the library is called
+    inp = make_inputs(small_case(1, 4, 300, 905))
+    g = to_device(inp, cuda_dev)
+    S_pad = sa.sage_padded_len(300)
+    for B, H, S, Sp in ((1, 3, 300, S_pad), (1, 4, 200, sa.sage_padded_len(200)), (1, 4, 299, S_pad)):
+        small = sa.Prepared.empty(B, H, S, Sp, cuda_dev)
+        with pytest.raises(sa.AttnError):
+            sa.sage_prepare_noalloc(g.q, g.k, g.v, small)
+    ok = sa.Prepared.empty(1, 4, 300, S_pad, cuda_dev)
+    ok.v_scale = ok.v_scale.to(torch.float64)
+    with pytest.raises(sa.AttnError):
+        sa.sage_prepare_noalloc(g.q, g.k, g.v, ok)
 
 
 def test_refuses_more_heads_than_its_scratch_holds():
