@@ -22,6 +22,10 @@ Functions and the passages they follow:
                     its tokens, subtracted before quantising K (ai-infra
                     handbook chapter above, section "SageAttention:
                     quantizing attention too").
+  quant_q_smooth -- Q smoothing (same section): each 32-row block's mean is
+                    subtracted before quantising Q and kept, in units of the
+                    block's step, as binary16 values that the score product
+                    adds back (the correction term qbar . k).
   quant_v        -- V to FP8 e4m3 transposed to [B, H, 128, S_pad], one FP32
                     scale per channel (same pull request, Technical Details).
   prepare        -- the three above in order, as the prepare stage runs them.
@@ -65,14 +69,20 @@ def lib():
                                       ctypes.c_float, c_p, c_p, c_p]
         L.oracle_k_mean.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, c_p]
         L.oracle_quant_v.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, c_p, c_p]
+        L.oracle_quant_q_smooth.argtypes = [c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                            ctypes.c_float, c_p, c_p, c_p]
+        L.oracle_f16_encode_array.argtypes = [c_p, c_p, ctypes.c_int64]
+        L.oracle_f16_decode.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_decode.restype = ctypes.c_double
         L.oracle_e4m3_encode_array.argtypes = [c_p, c_p, ctypes.c_int64]
         L.oracle_e4m3_decode_array.argtypes = [c_p, c_p, ctypes.c_int64]
         L.oracle_f32_to_bf16_array.argtypes = [c_p, c_p, ctypes.c_int64]
-        L.oracle_sage_attention.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, c_p,
-                                            ctypes.c_int]
-        L.oracle_sage_attention_v16.argtypes = [c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, c_p, ctypes.c_int]
+        L.oracle_sage_attention.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int,
+                                            ctypes.c_int, c_p, ctypes.c_int]
+        L.oracle_sage_attention_v16.argtypes = [c_p, c_p, c_p, c_p, c_p, c_p, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, c_p,
+                                                ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_init()
         _lib = L
@@ -162,6 +172,32 @@ def k_mean(x: torch.Tensor, S_pad: int) -> torch.Tensor:
     return torch.from_numpy(out)
 
 
+def quant_q_smooth(x: torch.Tensor, S_pad: int, scale_mult: float):
+    """Q smoothing: INT8 codes of fl32(x - block mean) [B, H, S_pad, 128], FP32 scales
+    [B, H, S_pad/32] (carrying scale_mult) and the block means in units of the block's
+    step as binary16 bit patterns (int16 tensor) [B, H, S_pad/32, 128]."""
+    B, S, H, D = x.shape
+    xb = _bf16_bits(x)
+    codes = np.empty((B, H, S_pad, 128), dtype=np.int8)
+    scales = np.empty((B, H, S_pad // 32), dtype=np.float32)
+    mean16 = np.empty((B, H, S_pad // 32, 128), dtype=np.uint16)
+    lib().oracle_quant_q_smooth(_ptr(xb), B, S, H, int(S_pad), float(np.float32(scale_mult)), _ptr(codes),
+                                _ptr(scales), _ptr(mean16))
+    return torch.from_numpy(codes), torch.from_numpy(scales), torch.from_numpy(mean16.view(np.int16))
+
+
+def f16_encode(x: np.ndarray) -> np.ndarray:
+    """binary64 -> binary16 bit patterns (uint16), nearest-even."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f16_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def f16_decode(h) -> float:
+    return float(lib().oracle_f16_decode(int(h) & 0xFFFF))
+
+
 def quant_v(x: torch.Tensor, S_pad: int):
     """e4m3 codes (uint8) [B, H, 128, S_pad] and FP32 scales [B, H, 128]."""
     B, S, H, D = x.shape
@@ -178,13 +214,14 @@ def padded_len(S: int) -> int:
 
 
 def prepare(q, k, v, softmax_scale, S_pad=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6,
-            rope_cos=None, rope_sin=None, rope_dim=0, smooth_k=False):
+            rope_cos=None, rope_sin=None, rope_dim=0, smooth_k=False, smooth_q=False):
     """The Sage prepare stage: optional norm/RoPE of Q and K, optional K
-    smoothing (subtract k_mean before quantising K), then the quantisers.
+    smoothing (subtract k_mean before quantising K), optional Q smoothing
+    (subtract each block's mean, kept as q_mean16), then the quantisers.
 
     Returns a dict with q_i8, k_i8, v_fp8 (uint8), q_scale, k_scale, v_scale,
-    the BF16 Q/K that were quantised (q_pre, k_pre) and k_mean (None unless
-    smooth_k).
+    the BF16 Q/K that were quantised (q_pre, k_pre), k_mean (None unless
+    smooth_k) and q_mean16 (None unless smooth_q).
     """
     B, S, H, D = q.shape
     if S_pad is None:
@@ -194,12 +231,22 @@ def prepare(q, k, v, softmax_scale, S_pad=None, q_norm_w=None, k_norm_w=None, rm
         q_pre = norm_rope(q, q_norm_w, rms_eps, rope_cos, rope_sin, rope_dim)
         k_pre = norm_rope(k, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim)
     c = softmax_log2_factor(softmax_scale)
-    q_i8, q_scale = quant_qk(q_pre, S_pad, c)
+    qm = None
+    if smooth_q:
+        q_i8, q_scale, qm = quant_q_smooth(q_pre, S_pad, c)
+    else:
+        q_i8, q_scale = quant_qk(q_pre, S_pad, c)
     km = k_mean(k_pre, S_pad) if smooth_k else None
     k_i8, k_scale = quant_qk(k_pre, S_pad, 1.0, km)
     v_fp8, v_scale = quant_v(v, S_pad)
     return dict(q_i8=q_i8, k_i8=k_i8, v_fp8=v_fp8, q_scale=q_scale, k_scale=k_scale, v_scale=v_scale,
-                q_pre=q_pre.contiguous(), k_pre=k_pre.contiguous(), S_pad=S_pad, log2_factor=c, k_mean=km)
+                q_pre=q_pre.contiguous(), k_pre=k_pre.contiguous(), S_pad=S_pad, log2_factor=c, k_mean=km,
+                q_mean16=qm)
+
+
+def _q_mean_arg(prep):
+    qm = prep.get("q_mean16")
+    return None if qm is None else np.ascontiguousarray(qm.numpy().view(np.uint16))
 
 
 def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool = False, p_e4m3: bool = False,
@@ -207,7 +254,8 @@ def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool =
     """FP64 attention of the prepared codes (dict as returned by prepare(), CPU
     tensors) for query rows (b, s, h) -> [n, 128] float64.  p_e4m3 also rounds
     the probabilities to e4m3 (448 * w) in the numerator, as the FP8 P V product
-    of the Sage forward needs; abs_v weights |V| instead of V."""
+    of the Sage forward needs; abs_v weights |V| instead of V.  With Q smoothing
+    (prep["q_mean16"]) Q's operand is f16(code + mean16), see oracle.c."""
     q8 = np.ascontiguousarray(prep["q_i8"].numpy())
     k8 = np.ascontiguousarray(prep["k_i8"].numpy())
     v8 = np.ascontiguousarray(prep["v_fp8"].numpy())
@@ -218,7 +266,9 @@ def sage_attention(prep: dict, S: int, rows: torch.Tensor, H: int, abs_v: bool =
     r = rows.to(torch.int64)
     flat = ((r[:, 0] * S + r[:, 1]) * H + r[:, 2]).contiguous().numpy()
     out = np.empty((len(flat), 128), dtype=np.float64)
-    lib().oracle_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs), _ptr(ks), _ptr(vs), B, S, H, int(S_pad),
+    qm = _q_mean_arg(prep)
+    lib().oracle_sage_attention(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs), _ptr(ks), _ptr(vs),
+                                _ptr(qm) if qm is not None else None, B, S, H, int(S_pad),
                                 _ptr(flat), len(flat), int(abs_v), int(p_e4m3), _ptr(out), int(nthreads))
     return out
 
@@ -238,8 +288,10 @@ def sage_attention_v16(prep: dict, v: torch.Tensor, rows: torch.Tensor, abs_v: b
     r = rows.to(torch.int64)
     flat = ((r[:, 0] * S + r[:, 1]) * H + r[:, 2]).contiguous().numpy()
     out = np.empty((len(flat), 128), dtype=np.float64)
-    lib().oracle_sage_attention_v16(_ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(vb), B, S, H, int(S_pad),
-                                    _ptr(flat), len(flat), int(abs_v), _ptr(out), int(nthreads))
+    qm = _q_mean_arg(prep)
+    lib().oracle_sage_attention_v16(_ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(qm) if qm is not None else None,
+                                    _ptr(vb), B, S, H, int(S_pad), _ptr(flat), len(flat), int(abs_v), _ptr(out),
+                                    int(nthreads))
     return out
 
 

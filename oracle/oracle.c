@@ -111,6 +111,43 @@ uint8_t oracle_e4m3_encode(float x) {
     return sign | (uint8_t)pick;
 }
 
+/* IEEE binary16: 1 sign bit, 5 exponent bits with bias 15, 10 mantissa bits;
+ * largest finite magnitude 65504, smallest subnormal 2^-24. */
+double oracle_f16_decode(uint16_t h) {
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 31) return m ? NAN : (s ? -INFINITY : INFINITY);
+    if (e == 0) v = m * ldexp(1.0, -24);
+    else v = (1.0 + m / 1024.0) * ldexp(1.0, e - 15);
+    return s ? -v : v;
+}
+
+/* Round a finite double to binary16, nearest, ties to the even pattern (magnitudes
+ * from halfway between 65504 and 2^16 up become infinity).  Bisection over the
+ * 31744 finite magnitudes, which increase with the pattern. */
+uint16_t oracle_f16_encode(double x) {
+    uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+    double a = fabs(x);
+    if (isnan(x)) return 0x7e00;
+    if (a >= 65520.0) return sign | 0x7c00;
+    int lo = 0, hi = 0x7c00;            /* invariant: value(lo) <= a < value(hi); value(0x7c00) := 2^16 */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (oracle_f16_decode((uint16_t)mid) <= a) lo = mid; else hi = mid;
+    }
+    double vh = (hi == 0x7c00) ? 65536.0 : oracle_f16_decode((uint16_t)hi);
+    double dl = a - oracle_f16_decode((uint16_t)lo), dh = vh - a;
+    int pick;
+    if (dl < dh) pick = lo;
+    else if (dh < dl) pick = hi;
+    else pick = (lo & 1) ? hi : lo;
+    return sign | (uint16_t)pick;
+}
+
+void oracle_f16_encode_array(const double* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_f16_encode(x[i]);
+}
+
 void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
     for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(x[i]);
 }
@@ -377,6 +414,101 @@ void oracle_k_mean(const uint16_t* x, int B, int S, int H, int64_t S_pad, float*
     }
 }
 
+/* ------------------------------------------- Sage prepare: Q smoothing */
+
+/*
+ * SageAttention subtracts the block means of Q as well as of K before the INT8
+ * quantisation (ai-infra handbook, "Kernel acceleration: attention, compilation
+ * and fusion", section "SageAttention: quantizing attention too").  For Q the
+ * mean does not cancel in the softmax: with q = (q - qbar_B) + qbar_B,
+ *   q . k_j = (q - qbar_B) . k_j + qbar_B . k_j,
+ * and the second term, the correction, differs from key to key.  It is kept
+ * with the block and added back in the score product.
+ *
+ * Readings (the page gives only the idea):
+ *   - the block is the format's 32-row quantisation block (rows < S only); its
+ *     mean per channel is summed in the order of oracle_k_mean's block sums,
+ *       P_g = (((0 + x[32j+g]) + x[32j+4+g]) + ...) + x[32j+28+g],  g = 0..3,
+ *       qbar[c] = ((P_0 + P_1) + (P_2 + P_3)) / n      (n = valid rows),
+ *     every + and the / in binary32;
+ *   - d = fl32(x - qbar[c]) is quantised like Q: a = max |d| over the block's
+ *     valid rows, code = clamp(rint(fl32(d * inv)), -127, 127);
+ *   - the mean is kept in units of the block's step, m[c] = qbar[c] * inv, as an
+ *     IEEE binary16 value m16[c] = f16(fl32(qbar[c] * inv)): the score product
+ *     takes Q's operand as the 16-bit value f16(code + m16) (see
+ *     oracle_sage_attention), so that operand is exact only up to binary16;
+ *   - to keep |m| within binary16's range the step is never below the block's
+ *     largest |qbar| over 256 x 127: the block uses a_eff = max(a, fl32(max_c
+ *     |qbar[c]| * 2^-8)), inv = fl32(127 / a_eff), scale = fl32(fl32(a_eff / 127)
+ *     * scale_mult), so |m| <= 32512 (1 + 2^-23);
+ *   - a block with a_eff = 0 (all zero), or whose 127 / a_eff overflows (a_eff
+ *     below 127 / FLT_MAX: every score it touches is below 1e-34), is stored as
+ *     zero codes, zero mean and scale 0; rows in [S, S_pad) are zero codes.
+ * codes: [B, H, S_pad, 128]; scales: [B, H, S_pad/32]; mean16: [B, H, S_pad/32, 128]
+ * binary16 bit patterns.
+ */
+void oracle_quant_q_smooth(const uint16_t* x, int B, int S, int H, int64_t S_pad, float scale_mult,
+                           int8_t* codes, float* scales, uint16_t* mean16) {
+    int64_t nblk = S_pad / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; b++) {
+        for (int h = 0; h < H; h++) {
+            for (int64_t j = 0; j < nblk; j++) {
+                int64_t r0 = 32 * j, r1 = r0 + 32 < S ? r0 + 32 : S;
+                int64_t n = r1 - r0;
+                int8_t* dst0 = codes + (((int64_t)b * H + h) * S_pad + r0) * 128;
+                uint16_t* m16 = mean16 + (((int64_t)b * H + h) * nblk + j) * 128;
+                float* sc = scales + ((int64_t)b * H + h) * nblk + j;
+                memset(dst0, 0, 32 * 128);
+                for (int c = 0; c < 128; c++) m16[c] = 0;
+                *sc = 0.0f;
+                if (n <= 0) continue;
+                float mu[128];
+                for (int c = 0; c < 128; c++) {
+                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    for (int g = 0; g < 4; g++)
+                        for (int t = 0; t < 8; t++) {
+                            int64_t s = r0 + 4 * t + g;
+                            if (s < S) part[g] = part[g] + oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]);
+                        }
+                    float blk = (part[0] + part[1]) + (part[2] + part[3]);
+                    mu[c] = blk / (float)n;
+                }
+                float a = 0.0f, cm = 0.0f;
+                for (int64_t s = r0; s < r1; s++)
+                    for (int c = 0; c < 128; c++) {
+                        float d = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]) - mu[c];
+                        if (fabsf(d) > a) a = fabsf(d);
+                    }
+                for (int c = 0; c < 128; c++)
+                    if (fabsf(mu[c]) > cm) cm = fabsf(mu[c]);
+                float floor_step = cm * (1.0f / 256.0f);
+                float ae = a > floor_step ? a : floor_step;
+                if (!(ae > 0.0f)) continue;
+                float inv = 127.0f / ae;
+                if (isinf(inv)) continue;
+                for (int64_t s = r0; s < r1; s++) {
+                    int8_t* dst = codes + (((int64_t)b * H + h) * S_pad + s) * 128;
+                    for (int c = 0; c < 128; c++) {
+                        float d = oracle_bf16_to_f32(x[(((int64_t)b * S + s) * H + h) * 128 + c]) - mu[c];
+                        float t = d * inv;
+                        float rq = rintf(t);
+                        if (rq > 127.0f) rq = 127.0f;
+                        if (rq < -127.0f) rq = -127.0f;
+                        dst[c] = (int8_t)rq;
+                    }
+                }
+                for (int c = 0; c < 128; c++) {
+                    float m = mu[c] * inv;
+                    m16[c] = oracle_f16_encode((double)m);
+                }
+                float st = ae / 127.0f;
+                *sc = st * scale_mult;
+            }
+        }
+    }
+}
+
 /* ----------------------------------------------- Sage prepare: V to e4m3 */
 
 /*
@@ -428,14 +560,30 @@ void oracle_quant_v(const uint16_t* x, int B, int S, int H, int64_t S_pad, uint8
  * P V product needs (same commit message: "FP8 WMMA for P V"); reading: the
  * weights w_j = 2^(t_j - max t) in (0, 1] enter the numerator as
  * e4m3(448 w_j) / 448 while the denominator sums the unrounded w_j.
+ * With Q smoothing (qm16 != NULL: [B, H, S_pad/32, 128] binary16 block means in
+ * step units, oracle_quant_q_smooth) q_i8[r, d] above is replaced by Q's 16-bit
+ * operand f16(q_i8[r, d] + qm16[r/32, d]) (q_operand), which carries the
+ * correction term qbar . k_j.
  * abs_v != 0 evaluates the same weights on |v| instead (the weighted mean
  * magnitude the rounding bounds of the tests scale with).
  * Layouts: codes [B, H, S_pad, 128] and [B, H, 128, S_pad], scales
  * [B, H, S_pad/32] and [B, H, 128].  rows: flattened (b*S + s)*H + h.
  */
+/* Q's operand of the score product for row r, channel d: the INT8 code, or with Q
+ * smoothing (qm16 != NULL, see oracle_quant_q_smooth) the binary16 value
+ * f16(code + m16[block, d]), the code and the block mean in step units summed
+ * exactly and rounded once. */
+static void q_operand(const int8_t* qrow, const uint16_t* qm16, double* qa) {
+    for (int d = 0; d < 128; d++) {
+        if (qm16) qa[d] = oracle_f16_decode(oracle_f16_encode((double)qrow[d] + oracle_f16_decode(qm16[d])));
+        else qa[d] = (double)qrow[d];
+    }
+}
+
 void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8, const float* qs,
-                           const float* ks, const float* vs, int B, int S, int H, int64_t S_pad, const int64_t* rows,
-                           int64_t n_rows, int abs_v, int p_e4m3, double* out, int nthreads) {
+                           const float* ks, const float* vs, const uint16_t* qm16, int B, int S, int H,
+                           int64_t S_pad, const int64_t* rows, int64_t n_rows, int abs_v, int p_e4m3, double* out,
+                           int nthreads) {
     int64_t nblk = S_pad / 32;
     (void)B;
     const int nt = oracle_team_size(nthreads);
@@ -451,13 +599,17 @@ void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8
             int64_t h = r % H, s = (r / H) % S, b = r / ((int64_t)H * S);
             int64_t bh = b * H + h;
             const int8_t* qrow = q8 + (bh * S_pad + s) * 128;
+            double qa[128];
+            q_operand(qrow, qm16 ? qm16 + (bh * nblk + s / 32) * 128 : NULL, qa);
             double fq = (double)qs[bh * nblk + s / 32];
             double tmax = -INFINITY;
             for (int64_t j = 0; j < S; j++) {
                 const int8_t* krow = k8 + (bh * S_pad + j) * 128;
-                int64_t dot = 0;
-                for (int d = 0; d < 128; d++) dot += (int64_t)qrow[d] * (int64_t)krow[d];
-                t[j] = (double)dot * fq * (double)ks[bh * nblk + j / 32];
+                /* binary64: exact for integer codes; with the 16-bit operand every product is
+                   exact and the sum carries at most a 2^-53 relative rounding */
+                double dot = 0.0;
+                for (int d = 0; d < 128; d++) dot += qa[d] * (double)krow[d];
+                t[j] = dot * fq * (double)ks[bh * nblk + j / 32];
                 if (t[j] > tmax) tmax = t[j];
             }
             double wsum = 0.0;
@@ -485,12 +637,12 @@ void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8
  * V taken from the BF16 input itself (no V quantisation):
  *   O[r, d] = sum_{j < S} 2^(t_j - max t) v[j, d] / sum_{j < S} 2^(t_j - max t),
  *   v[j, d] = the BF16 V of (b, j, h, d)
- * with t_j as in oracle_sage_attention and nothing rounded.  v: [B, S, H, 128]
- * BF16 bits.  abs_v != 0 weights |v| instead.
+ * with t_j as in oracle_sage_attention (Q smoothing through qm16 as there) and
+ * nothing rounded.  v: [B, S, H, 128] BF16 bits.  abs_v != 0 weights |v| instead.
  */
 void oracle_sage_attention_v16(const int8_t* q8, const int8_t* k8, const float* qs, const float* ks,
-                               const uint16_t* v, int B, int S, int H, int64_t S_pad, const int64_t* rows,
-                               int64_t n_rows, int abs_v, double* out, int nthreads) {
+                               const uint16_t* qm16, const uint16_t* v, int B, int S, int H, int64_t S_pad,
+                               const int64_t* rows, int64_t n_rows, int abs_v, double* out, int nthreads) {
     int64_t nblk = S_pad / 32;
     (void)B;
     const int nt = oracle_team_size(nthreads);
@@ -505,13 +657,17 @@ void oracle_sage_attention_v16(const int8_t* q8, const int8_t* k8, const float* 
             int64_t h = r % H, s = (r / H) % S, b = r / ((int64_t)H * S);
             int64_t bh = b * H + h;
             const int8_t* qrow = q8 + (bh * S_pad + s) * 128;
+            double qa[128];
+            q_operand(qrow, qm16 ? qm16 + (bh * nblk + s / 32) * 128 : NULL, qa);
             double fq = (double)qs[bh * nblk + s / 32];
             double tmax = -INFINITY;
             for (int64_t j = 0; j < S; j++) {
                 const int8_t* krow = k8 + (bh * S_pad + j) * 128;
-                int64_t dot = 0;
-                for (int d = 0; d < 128; d++) dot += (int64_t)qrow[d] * (int64_t)krow[d];
-                t[j] = (double)dot * fq * (double)ks[bh * nblk + j / 32];
+                /* binary64: exact for integer codes; with the 16-bit operand every product is
+                   exact and the sum carries at most a 2^-53 relative rounding */
+                double dot = 0.0;
+                for (int d = 0; d < 128; d++) dot += qa[d] * (double)krow[d];
+                t[j] = dot * fq * (double)ks[bh * nblk + j / 32];
                 if (t[j] > tmax) tmax = t[j];
             }
             double wsum = 0.0;
