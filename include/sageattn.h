@@ -29,8 +29,10 @@
  *                   the caller's workspace.
  *
  * Beyond those: sage_prepare_smooth_k (K smoothing before the INT8
- * quantisation) and sage_attn_fwd_pv16 (P V in 16 bits with V unquantised),
- * both from the handbook's SageAttention section; sage_prepare_noalloc (no
+ * quantisation), sage_prepare_smoothed with sage_attn_fwd_smooth_q and
+ * sage_attn_fwd_pv16_smooth_q (Q smoothing with its correction term) and
+ * sage_attn_fwd_pv16 (P V in 16 bits with V unquantised), all from the
+ * handbook's SageAttention section; sage_prepare_noalloc (no
  * workspace argument); attn_selftest_wait_timeout (exercises the failure path);
  * attn_sm_clock_sample (SM clock counters, for timing);
  * sizes and status helpers.
@@ -197,6 +199,45 @@ ATTN_API attn_status sage_prepare_smooth_k(const void* q, const void* k, const v
                                   attn_stream_t stream);
 
 /*
+ * sage_prepare_smoothed -- sage_prepare with Q smoothing, K smoothing or both.
+ * SageAttention subtracts the block means of Q as well as of K before the INT8
+ * quantisation (ai-infra handbook, "Kernel acceleration: attention, compilation
+ * and fusion", section "SageAttention: quantizing attention too").  K's mean
+ * cancels in the softmax (sage_prepare_smooth_k).  Q's does not: with
+ * q = (q - qbar) + qbar, q . k_j = (q - qbar) . k_j + qbar . k_j, and the
+ * correction term qbar . k_j differs from key to key, so the mean is kept with
+ * its block and added back in the score product (sage_attn_fwd_smooth_q).
+ *   All arguments as sage_prepare_smooth_k, plus
+ *   smooth_q, smooth_k : 0 or 1 each.
+ *   q_mean     : with smooth_q, binary16 [B, H, S_pad/32, 128] output (16-byte
+ *                aligned): each 32-row block's per-channel mean of Q' (Q after
+ *                the optional RMSNorm + RoPE), in units of the block's step,
+ *                m[c] = f16(fl32(qbar[c] * inv)).  qbar[c] is the block sum in
+ *                k_mean's fixed order (four partial sums over rows 32j+4t+g,
+ *                (P_0 + P_1) + (P_2 + P_3)) divided by the block's valid rows.
+ *   q_i8, q_scale : with smooth_q, the codes of d = fl32(Q' - qbar[c]); the step
+ *                is a_eff / 127 with a_eff = max(max |d|, max_c |qbar[c]| / 256)
+ *                (so |m| <= 32512 stays in binary16), inv = fl32(127 / a_eff),
+ *                q_scale = fl32(fl32(a_eff / 127) * c).  An all-zero block, or
+ *                one whose 127 / a_eff overflows (every |Q'| below about
+ *                3.7e-37), is stored as zero codes, zero means and scale 0.
+ *   k_mean     : with smooth_k, as sage_prepare_smooth_k (else not written).
+ *   workspace  : sage_prepare_smooth_k_workspace_size(B, H, S_pad) bytes with
+ *                smooth_k, else sage_prepare_workspace_size(B, H).
+ * Outputs not affected by a flag are those of sage_prepare, bit for bit.
+ * Errors as sage_prepare_smooth_k; a flag other than 0/1, or a NULL q_mean
+ * (k_mean) with smooth_q (smooth_k) -> ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API attn_status sage_prepare_smoothed(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                           const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                           float softmax_scale, const void* q_norm_w, const void* k_norm_w,
+                                           float rms_eps, const void* rope_cos, const void* rope_sin, int rope_dim,
+                                           int64_t S_pad, int smooth_q, int smooth_k, int8_t* q_i8, int8_t* k_i8,
+                                           uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
+                                           void* q_mean, float* k_mean, void* workspace, size_t workspace_bytes,
+                                           attn_stream_t stream);
+
+/*
  * sage_prepare_noalloc -- sage_prepare without a workspace argument.  None of the
  * pages has a counterpart; it exists for callers that cannot allocate device
  * memory when they call us: code whose device memory is owned and budgeted by
@@ -281,9 +322,34 @@ ATTN_API attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, 
                                         void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * sage_attn_fwd_smooth_q, sage_attn_fwd_pv16_smooth_q -- sage_attn_fwd and
+ * sage_attn_fwd_pv16 on tensors prepared with Q smoothing (sage_prepare_smoothed,
+ * smooth_q = 1).  Q's operand of the score product is the binary16 value
+ * f16(q_i8[r, d] + q_mean[r/32, d]) -- the code and the block mean in step
+ * units, summed and rounded once -- so that
+ *   t[r, j] = (sum_d f16(q_i8[r,d] + q_mean[r/32,d]) k_i8[j,d]) * q_scale[r/32] * k_scale[j/32]
+ * carries the correction term qbar . k_j; the FP32 accumulation of that sum is
+ * exact while it stays below 2^24 in magnitude.  The rest is as sage_attn_fwd
+ * (resp. sage_attn_fwd_pv16).
+ *   q_mean : const binary16 [B, H, S_pad/32, 128], 16-byte aligned
+ * Enqueues three kernels on `stream`.  Errors as sage_attn_fwd (resp.
+ * sage_attn_fwd_pv16); q_mean NULL -> ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API attn_status sage_attn_fwd_smooth_q(const int8_t* q_i8, const void* q_mean, const int8_t* k_i8,
+                                            const uint8_t* v_fp8, const float* q_scale, const float* k_scale,
+                                            const float* v_scale, void* o, const int64_t o_str[3], int B, int S,
+                                            int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                                            attn_stream_t stream);
+ATTN_API attn_status sage_attn_fwd_pv16_smooth_q(const int8_t* q_i8, const void* q_mean, const int8_t* k_i8,
+                                                 const float* q_scale, const float* k_scale, const void* v,
+                                                 const int64_t v_str[3], void* o, const int64_t o_str[3], int B,
+                                                 int S, int H, int D, int64_t S_pad, void* workspace,
+                                                 size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * sage_attention_workspace_size -- bytes of device scratch sage_attention needs
  * (0 for an empty problem).  smooth_k, pv_bf16 and q_on_load as given to
- * sage_attention.
+ * sage_attention (the size does not depend on smooth_q).
  */
 ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16,
                                               int q_on_load);
@@ -303,6 +369,9 @@ ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int s
  * passes), so it is not the default.  Either way the output is bit-identical to
  * the two-call sequence.
  *   q, k, v, strides, softmax_scale, RMSNorm and RoPE arguments : as sage_prepare
+ *   smooth_q   : 0 or 1 -- Q smoothing as sage_prepare_smoothed (the FP16 Q operand
+ *                written to the workspace is then f16(code + block mean)); not
+ *                with q_on_load (ATTN_ERR_UNSUPPORTED)
  *   smooth_k   : 0 or 1 -- K smoothing as sage_prepare_smooth_k
  *   pv_bf16    : 0 -- P and V in e4m3 (sage_attn_fwd); 1 -- P in BF16 times the
  *                BF16 V input (sage_attn_fwd_pv16; V is then not quantised)
@@ -313,15 +382,15 @@ ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int s
  *                smooth_k, pv_bf16, q_on_load) bytes, 16-byte aligned; contents
  *                on entry do not matter.
  * Enqueues the prepare kernels (one to four) and the attention kernel on
- * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_k, pv_bf16 or
- * q_on_load other than 0/1 -> ATTN_ERR_INVALID_ARG.
+ * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_q, smooth_k,
+ * pv_bf16 or q_on_load other than 0/1 -> ATTN_ERR_INVALID_ARG.
  */
 ATTN_API attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                                     const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                                     float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
-                                    const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_k,
-                                    int pv_bf16, int q_on_load, void* o, const int64_t o_str[3], void* workspace,
-                                    size_t workspace_bytes, attn_stream_t stream);
+                                    const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_q,
+                                    int smooth_k, int pv_bf16, int q_on_load, void* o, const int64_t o_str[3],
+                                    void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_get_device_status -- synchronise `stream`, then read and clear the

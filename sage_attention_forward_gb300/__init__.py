@@ -83,7 +83,17 @@ def lib() -> ctypes.CDLL:
         L.sage_attention_workspace_size.argtypes = [i, i, ctypes.c_int64, i, i, i]
         L.sage_attention_workspace_size.restype = ctypes.c_size_t
         L.sage_attention.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp, _vp,
-                                     ctypes.c_float, _vp, _vp, i, i, i, i, _vp, _I64x3, _vp, ctypes.c_size_t, _vp]
+                                     ctypes.c_float, _vp, _vp, i, i, i, i, i, _vp, _I64x3, _vp, ctypes.c_size_t, _vp]
+        L.sage_prepare_smoothed.argtypes = [_vp, _vp, _vp, i, i, i, i, _I64x3, _I64x3, _I64x3, ctypes.c_float, _vp,
+                                            _vp, ctypes.c_float, _vp, _vp, i, ctypes.c_int64, i, i, _vp, _vp, _vp,
+                                            _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.sage_prepare_smoothed.restype = i
+        L.sage_attn_fwd_smooth_q.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _I64x3, i, i, i, i,
+                                             ctypes.c_int64, _vp, ctypes.c_size_t, _vp]
+        L.sage_attn_fwd_smooth_q.restype = i
+        L.sage_attn_fwd_pv16_smooth_q.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _I64x3, _vp, _I64x3, i, i, i, i,
+                                                  ctypes.c_int64, _vp, ctypes.c_size_t, _vp]
+        L.sage_attn_fwd_pv16_smooth_q.restype = i
         L.sage_attention.restype = i
         L.attn_selftest_wait_timeout.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.attn_selftest_wait_timeout.restype = i
@@ -153,6 +163,8 @@ class Prepared:
     S: int
     S_pad: int
     k_mean: torch.Tensor | None = None   # fp32 [B, H, 128], set when K was smoothed
+    q_mean: torch.Tensor | None = None   # fp16 [B, H, S_pad / 32, 128], set when Q was smoothed: each
+                                         # block's mean in units of its step
 
     @staticmethod
     def empty(B: int, H: int, S: int, S_pad: int, device) -> "Prepared":
@@ -176,6 +188,8 @@ def _check_prepared(out: Prepared, q: torch.Tensor, S_pad: int | None = None) ->
             "k_scale": ((B, H, S_pad // 32), torch.float32), "v_scale": ((B, H, 128), torch.float32)}
     if out.k_mean is not None:
         want["k_mean"] = ((B, H, 128), torch.float32)
+    if out.q_mean is not None:
+        want["q_mean"] = ((B, H, S_pad // 32, 128), torch.float16)
     for name, (shape, dtype) in want.items():
         t = getattr(out, name)
         if tuple(t.shape) != shape or t.dtype != dtype:
@@ -202,10 +216,12 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
                  S_pad: int | None = None, q_norm_w: torch.Tensor | None = None,
                  k_norm_w: torch.Tensor | None = None, rms_eps: float = 1e-6, rope_cos: torch.Tensor | None = None,
                  rope_sin: torch.Tensor | None = None, rope_dim: int = 0, out: Prepared | None = None,
-                 workspace: torch.Tensor | None = None, stream=None, smooth_k: bool = False) -> Prepared:
+                 workspace: torch.Tensor | None = None, stream=None, smooth_k: bool = False,
+                 smooth_q: bool = False) -> Prepared:
     """Quantise Q/K to INT8 and V to e4m3 (optionally RMSNorm + RoPE on Q/K first;
     with smooth_k, K's per-channel token mean is subtracted before quantising K
-    and returned in out.k_mean)."""
+    and returned in out.k_mean; with smooth_q, each 32-row block's mean is
+    subtracted from Q and returned, in step units, in out.q_mean)."""
     B, S, H, D = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
@@ -215,6 +231,10 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
         out = Prepared.empty(B, H, S, S_pad, q.device)
     if smooth_k and out.k_mean is None:
         out.k_mean = torch.empty((B, H, 128), dtype=torch.float32, device=q.device)
+    if smooth_q and out.q_mean is None:
+        out.q_mean = torch.empty((B, H, S_pad // 32, 128), dtype=torch.float16, device=q.device)
+    if not smooth_q:
+        out.q_mean = None
     _check_prepared(out, q, S_pad)
     if workspace is None:
         workspace = prepare_workspace(B, H, q.device, S_pad, smooth_k)
@@ -223,6 +243,15 @@ def sage_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scal
     def ptr(t):
         return None if t is None else t.data_ptr()
 
+    if smooth_q:
+        _check(lib().sage_prepare_smoothed(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
+                                           float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps),
+                                           ptr(rope_cos), ptr(rope_sin), int(rope_dim), int(S_pad), 1, int(smooth_k),
+                                           out.q_i8.data_ptr(), out.k_i8.data_ptr(), out.v_fp8.data_ptr(),
+                                           out.q_scale.data_ptr(), out.k_scale.data_ptr(), out.v_scale.data_ptr(),
+                                           out.q_mean.data_ptr(), ptr(out.k_mean) if smooth_k else None,
+                                           workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+        return out
     if smooth_k:
         _check(lib().sage_prepare_smooth_k(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                                            float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps),
@@ -281,6 +310,12 @@ def sage_attn_fwd(prep: Prepared, out: torch.Tensor | None = None, workspace: to
     if workspace is None:
         workspace = attn_workspace(B, H, S_pad, prep.q_i8.device)
     os_ = _bshd("out", out)
+    if prep.q_mean is not None:
+        _check(lib().sage_attn_fwd_smooth_q(prep.q_i8.data_ptr(), prep.q_mean.data_ptr(), prep.k_i8.data_ptr(),
+                                            prep.v_fp8.data_ptr(), prep.q_scale.data_ptr(), prep.k_scale.data_ptr(),
+                                            prep.v_scale.data_ptr(), out.data_ptr(), os_, B, S, H, D, int(S_pad),
+                                            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+        return out
     _check(lib().sage_attn_fwd(prep.q_i8.data_ptr(), prep.k_i8.data_ptr(), prep.v_fp8.data_ptr(),
                                prep.q_scale.data_ptr(), prep.k_scale.data_ptr(), prep.v_scale.data_ptr(),
                                out.data_ptr(), os_, B, S, H, D, int(S_pad), workspace.data_ptr(), workspace.numel(),
@@ -299,6 +334,12 @@ def sage_attn_fwd_pv16(prep: Prepared, v: torch.Tensor, out: torch.Tensor | None
     if workspace is None:
         workspace = attn_workspace(B, H, S_pad, prep.q_i8.device)
     vs, os_ = _bshd("v", v), _bshd("out", out)
+    if prep.q_mean is not None:
+        _check(lib().sage_attn_fwd_pv16_smooth_q(prep.q_i8.data_ptr(), prep.q_mean.data_ptr(), prep.k_i8.data_ptr(),
+                                                 prep.q_scale.data_ptr(), prep.k_scale.data_ptr(), v.data_ptr(), vs,
+                                                 out.data_ptr(), os_, B, S, H, D, int(S_pad), workspace.data_ptr(),
+                                                 workspace.numel(), _stream_ptr(stream)))
+        return out
     _check(lib().sage_attn_fwd_pv16(prep.q_i8.data_ptr(), prep.k_i8.data_ptr(), prep.q_scale.data_ptr(),
                                     prep.k_scale.data_ptr(), v.data_ptr(), vs, out.data_ptr(), os_, B, S, H, D,
                                     int(S_pad), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
@@ -314,13 +355,14 @@ def sage_attention_workspace(B: int, H: int, S: int, device, smooth_k: bool = Fa
 
 def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
                    rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3",
-                   workspace=None, q_on_load=False) -> torch.Tensor:
+                   workspace=None, q_on_load=False, smooth_q=False) -> torch.Tensor:
     """Prepare + attention in one library call: the SageAttention-style forward of BF16 Q/K/V.
 
     pv="e4m3": P and V in FP8; pv="bf16": P in BF16 times the unquantised V.  The
     prepared tensors stay in `workspace` (allocated here unless given).  q_on_load:
     Q is coded by the forward as it loads it instead of by the prepare (the same
-    output; slower on a GB300)."""
+    output; slower on a GB300).  smooth_q / smooth_k: block-mean smoothing of Q
+    (with its correction term) / sequence-mean smoothing of K before INT8."""
     if pv not in ("e4m3", "bf16"):
         raise ValueError(f"pv must be 'e4m3' or 'bf16', not {pv!r}")
     B, S, H, D = q.shape
@@ -337,7 +379,7 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
 
     _check(lib().sage_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                                 float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
-                                ptr(rope_sin), int(rope_dim), int(bool(smooth_k)), int(pv == "bf16"),
+                                ptr(rope_sin), int(rope_dim), int(bool(smooth_q)), int(bool(smooth_k)), int(pv == "bf16"),
                                 int(bool(q_on_load)), out.data_ptr(), os_, workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
     return out
 

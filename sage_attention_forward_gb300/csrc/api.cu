@@ -332,7 +332,7 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
                          const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad, int8_t* q_i8,
                          int8_t* k_i8, uint8_t* v_fp8, float* q_scale, float* k_scale, float* v_scale,
                          void* workspace, size_t workspace_bytes, size_t workspace_needed, float* k_mean,
-                         attn_stream_t stream) {
+                         void* q_mean16, attn_stream_t stream) {
   bool empty = false;
   TRY(check_shape(B, S, H, D, &empty));
   if (empty) return ATTN_OK;
@@ -347,6 +347,7 @@ static attn_status prepare_checked(const char* who, const void* q, const void* k
                 workspace_needed);
   TRY(check_device());
   a.vmax = reinterpret_cast<uint32_t*>(workspace);
+  a.q_mean16 = q_mean16;
   if (k_mean != nullptr) {
     a.k_mean = k_mean;
     // block sums after the V maxima, 16-byte aligned (B*H*128 words is a multiple of 4)
@@ -366,7 +367,7 @@ attn_status sage_prepare(const void* q, const void* k, const void* v, int B, int
   return prepare_checked("sage_prepare", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale, q_norm_w,
                          k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8, q_scale,
                          k_scale, v_scale, workspace, workspace_bytes, sage_prepare_workspace_size(B, H), nullptr,
-                         stream);
+                         nullptr, stream);
 }
 
 attn_status sage_prepare_noalloc(const void* q, const void* k, const void* v, int B, int S, int H, int D,
@@ -419,7 +420,34 @@ attn_status sage_prepare_smooth_k(const void* q, const void* k, const void* v, i
   return prepare_checked("sage_prepare_smooth_k", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale,
                          q_norm_w, k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8,
                          q_scale, k_scale, v_scale, workspace, workspace_bytes,
-                         sage_prepare_smooth_k_workspace_size(B, H, S_pad), k_mean, stream);
+                         sage_prepare_smooth_k_workspace_size(B, H, S_pad), k_mean, nullptr, stream);
+}
+
+attn_status sage_prepare_smoothed(const void* q, const void* k, const void* v, int B, int S, int H, int D,
+                                  const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                                  float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
+                                  const void* rope_cos, const void* rope_sin, int rope_dim, int64_t S_pad,
+                                  int smooth_q, int smooth_k, int8_t* q_i8, int8_t* k_i8, uint8_t* v_fp8,
+                                  float* q_scale, float* k_scale, float* v_scale, void* q_mean, float* k_mean,
+                                  void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  bool empty = false;
+  TRY(check_shape(B, S, H, D, &empty));
+  if (empty) return ATTN_OK;
+  if ((smooth_q != 0 && smooth_q != 1) || (smooth_k != 0 && smooth_k != 1))
+    return fail(ATTN_ERR_INVALID_ARG, "smooth_q=%d and smooth_k=%d must be 0 or 1", smooth_q, smooth_k);
+  if (smooth_q) {
+    if (q_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "sage_prepare_smoothed: smooth_q needs q_mean");
+    if (!aligned16(q_mean)) return fail(ATTN_ERR_ALIGNMENT, "sage_prepare_smoothed: q_mean is not 16-byte aligned");
+  }
+  if (smooth_k) {
+    if (k_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "sage_prepare_smoothed: smooth_k needs k_mean");
+    if (!aligned16(k_mean)) return fail(ATTN_ERR_ALIGNMENT, "sage_prepare_smoothed: k_mean is not 16-byte aligned");
+  }
+  const size_t need = smooth_k ? sage_prepare_smooth_k_workspace_size(B, H, S_pad) : sage_prepare_workspace_size(B, H);
+  return prepare_checked("sage_prepare_smoothed", q, k, v, B, S, H, D, q_str, k_str, v_str, softmax_scale, q_norm_w,
+                         k_norm_w, rms_eps, rope_cos, rope_sin, rope_dim, S_pad, q_i8, k_i8, v_fp8, q_scale, k_scale,
+                         v_scale, workspace, workspace_bytes, need, smooth_k ? k_mean : nullptr,
+                         smooth_q ? q_mean : nullptr, stream);
 }
 
 size_t sage_attn_workspace_size(int B, int H, int64_t S_pad) {
@@ -427,10 +455,13 @@ size_t sage_attn_workspace_size(int B, int H, int64_t S_pad) {
   return (size_t)4 * (size_t)B * (size_t)H * (size_t)S_pad * 128;
 }
 
-attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t* v_fp8, const float* q_scale,
-                          const float* k_scale, const float* v_scale, void* o, const int64_t o_str[3], int B,
-                          int S, int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
-                          attn_stream_t stream) {
+// The two-call forwards: the codes widened to the FP16 score operands (Q's carrying its
+// block means with Q smoothing), then the attention kernel in the chosen P V mode.
+static attn_status attn_fwd_prepared(const char* who, const int8_t* q_i8, const void* q_mean, const int8_t* k_i8,
+                                     const float* q_scale, const float* k_scale, const uint8_t* v_fp8,
+                                     const float* v_scale, const void* v, const int64_t v_str[3], int pv_bf16,
+                                     void* o, const int64_t o_str[3], int B, int S, int H, int D, int64_t S_pad,
+                                     void* workspace, size_t workspace_bytes, attn_stream_t stream) {
   bool empty = false;
   TRY(check_shape(B, S, H, D, &empty));
   if (empty) return ATTN_OK;
@@ -438,54 +469,15 @@ attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t*
     return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
   if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
   TRY(check_grid(B, H, S_pad));
-  struct {
+  struct In {
     const char* n;
     const void* p;
-  } ins[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"v_fp8", v_fp8}, {"q_scale", q_scale}, {"k_scale", k_scale},
-             {"v_scale", v_scale}, {"workspace", workspace}};
-  for (auto& t : ins) {
-    if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
-    if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
-  }
-  if (workspace_bytes < sage_attn_workspace_size(B, H, S_pad))
-    return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
-                sage_attn_workspace_size(B, H, S_pad));
-  long long os[3];
-  TRY(check_strides("o", o, o_str, B, S, H, os));
-  TRY(check_device());
-  TRY(get_encoder());
-  const long long bh = (long long)B * H;
-  const long long n_codes = bh * S_pad * 128;
-  uint8_t* q16 = reinterpret_cast<uint8_t*>(workspace);
-  uint8_t* k16 = q16 + 2 * n_codes;
-  CUtensorMap tq, tk, tv;
-  TRY(tmap_f16_rows(&tq, q16, S_pad, bh));
-  TRY(tmap_f16_rows(&tk, k16, S_pad, bh));
-  TRY(tmap_bytes_3d(&tv, v_fp8, S_pad, 128, bh));
-  cudaError_t e = sa::launch_sage_widen(q_i8, k_i8, q16, k16, n_codes, sa::device_sm_count(), (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd widen launch");
-  e = sa::launch_sage_attn(tq, tk, tv, q_scale, k_scale, v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
-                           (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd launch");
-  return ATTN_OK;
-}
-
-attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale, const float* k_scale,
-                               const void* v, const int64_t v_str[3], void* o, const int64_t o_str[3], int B, int S,
-                               int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
-                               attn_stream_t stream) {
-  bool empty = false;
-  TRY(check_shape(B, S, H, D, &empty));
-  if (empty) return ATTN_OK;
-  if (S_pad < S || S_pad % 128 != 0)
-    return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld must be a multiple of 128 and >= S=%d", (long long)S_pad, S);
-  if (S_pad > (1ll << 31) - 256) return fail(ATTN_ERR_INVALID_ARG, "S_pad=%lld too large", (long long)S_pad);
-  TRY(check_grid(B, H, S_pad));
-  struct {
-    const char* n;
-    const void* p;
-  } ins[] = {{"q_i8", q_i8}, {"k_i8", k_i8}, {"q_scale", q_scale}, {"k_scale", k_scale}, {"workspace", workspace}};
-  for (auto& t : ins) {
+    bool needed;
+  } ins[] = {{"q_i8", q_i8, true},        {"k_i8", k_i8, true},          {"q_scale", q_scale, true},
+             {"k_scale", k_scale, true},  {"workspace", workspace, true}, {"v_fp8", v_fp8, !pv_bf16},
+             {"v_scale", v_scale, !pv_bf16}, {"q_mean", q_mean, q_mean != nullptr}};
+  for (const In& t : ins) {
+    if (!t.needed) continue;
     if (!t.p) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", t.n);
     if (!aligned16(t.p)) return fail(ATTN_ERR_ALIGNMENT, "%s is not 16-byte aligned", t.n);
   }
@@ -493,7 +485,7 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
     return fail(ATTN_ERR_INVALID_ARG, "workspace_bytes=%zu < %zu required", workspace_bytes,
                 sage_attn_workspace_size(B, H, S_pad));
   long long vs[3], os[3];
-  TRY(check_strides("v", v, v_str, B, S, H, vs));
+  if (pv_bf16) TRY(check_strides("v", v, v_str, B, S, H, vs));
   TRY(check_strides("o", o, o_str, B, S, H, os));
   TRY(check_device());
   TRY(get_encoder());
@@ -504,20 +496,62 @@ attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const flo
   CUtensorMap tq, tk, tv;
   TRY(tmap_f16_rows(&tq, q16, S_pad, bh));
   TRY(tmap_f16_rows(&tk, k16, S_pad, bh));
-  TRY(tmap_bhsd_bf16(&tv, v, B, S, H, vs));
+  if (pv_bf16) TRY(tmap_bhsd_bf16(&tv, v, B, S, H, vs));
+  else TRY(tmap_bytes_3d(&tv, v_fp8, S_pad, 128, bh));
   cudaError_t e = sa::launch_sage_widen(q_i8, k_i8, q16, k16, n_codes, sa::device_sm_count(), (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd_pv16 widen launch");
-  e = sa::launch_sage_attn_pv16(tq, tk, tv, q_scale, k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
-                                (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "sage_attn_fwd_pv16 launch");
+  if (e == cudaSuccess && q_mean != nullptr)   // Q's operand again, now with its block means
+    e = sa::launch_widen_q_mean(q_i8, q_mean, q16, n_codes, sa::device_sm_count(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, who);
+  if (pv_bf16)
+    e = sa::launch_sage_attn_pv16(tq, tk, tv, q_scale, k_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                  (cudaStream_t)stream);
+  else
+    e = sa::launch_sage_attn(tq, tk, tv, q_scale, k_scale, v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                             (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, who);
   return ATTN_OK;
+}
+
+attn_status sage_attn_fwd(const int8_t* q_i8, const int8_t* k_i8, const uint8_t* v_fp8, const float* q_scale,
+                          const float* k_scale, const float* v_scale, void* o, const int64_t o_str[3], int B,
+                          int S, int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream) {
+  return attn_fwd_prepared("sage_attn_fwd", q_i8, nullptr, k_i8, q_scale, k_scale, v_fp8, v_scale, nullptr, nullptr,
+                           0, o, o_str, B, S, H, D, S_pad, workspace, workspace_bytes, stream);
+}
+
+attn_status sage_attn_fwd_pv16(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale, const float* k_scale,
+                               const void* v, const int64_t v_str[3], void* o, const int64_t o_str[3], int B, int S,
+                               int H, int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                               attn_stream_t stream) {
+  return attn_fwd_prepared("sage_attn_fwd_pv16", q_i8, nullptr, k_i8, q_scale, k_scale, nullptr, nullptr, v, v_str,
+                           1, o, o_str, B, S, H, D, S_pad, workspace, workspace_bytes, stream);
+}
+
+attn_status sage_attn_fwd_smooth_q(const int8_t* q_i8, const void* q_mean, const int8_t* k_i8,
+                                   const uint8_t* v_fp8, const float* q_scale, const float* k_scale,
+                                   const float* v_scale, void* o, const int64_t o_str[3], int B, int S, int H, int D,
+                                   int64_t S_pad, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (q_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "q_mean is NULL");
+  return attn_fwd_prepared("sage_attn_fwd_smooth_q", q_i8, q_mean, k_i8, q_scale, k_scale, v_fp8, v_scale, nullptr,
+                           nullptr, 0, o, o_str, B, S, H, D, S_pad, workspace, workspace_bytes, stream);
+}
+
+attn_status sage_attn_fwd_pv16_smooth_q(const int8_t* q_i8, const void* q_mean, const int8_t* k_i8,
+                                        const float* q_scale, const float* k_scale, const void* v,
+                                        const int64_t v_str[3], void* o, const int64_t o_str[3], int B, int S, int H,
+                                        int D, int64_t S_pad, void* workspace, size_t workspace_bytes,
+                                        attn_stream_t stream) {
+  if (q_mean == nullptr) return fail(ATTN_ERR_INVALID_ARG, "q_mean is NULL");
+  return attn_fwd_prepared("sage_attn_fwd_pv16_smooth_q", q_i8, q_mean, k_i8, q_scale, k_scale, nullptr, nullptr, v,
+                           v_str, 1, o, o_str, B, S, H, D, S_pad, workspace, workspace_bytes, stream);
 }
 
 // Workspace of sage_attention: consecutive 256-byte aligned pieces.
 // The one-call op's workspace: Q's FP16 codes and scales (unless the forward codes Q
 // as it loads it), K's, V's codes and scales (FP8 mode), the smoothing buffers.
 struct FusedLayout {
-  size_t q16, q_scale, k16, k_scale, v_fp8, v_scale, vmax, k_mean, k_partial, total;
+  size_t q16, q_scale, q_mean, k16, k_scale, v_fp8, v_scale, vmax, k_mean, k_partial, total;
 };
 static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int pv_bf16, int q_on_load) {
   FusedLayout L{};
@@ -531,6 +565,7 @@ static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int p
   if (!q_on_load) {
     L.q16 = take(bh * (size_t)S_pad * 128 * 2);
     L.q_scale = take(bh * nblk * 4);
+    L.q_mean = take(bh * nblk * 128 * 2);   // used with Q smoothing only
   }
   L.k16 = take(bh * (size_t)S_pad * 128 * 2);
   L.k_scale = take(bh * nblk * 4);
@@ -555,15 +590,18 @@ size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int smooth_k, 
 attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
                            float softmax_scale, const void* q_norm_w, const void* k_norm_w, float rms_eps,
-                           const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_k, int pv_bf16,
-                           int q_on_load, void* o, const int64_t o_str[3], void* workspace, size_t workspace_bytes,
-                           attn_stream_t stream) {
+                           const void* rope_cos, const void* rope_sin, int rope_dim, int smooth_q, int smooth_k,
+                           int pv_bf16, int q_on_load, void* o, const int64_t o_str[3], void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream) {
   bool empty = false;
   TRY(check_shape(B, S, H, D, &empty));
   if (empty) return ATTN_OK;
-  if ((smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1) || (q_on_load != 0 && q_on_load != 1))
-    return fail(ATTN_ERR_INVALID_ARG, "smooth_k=%d, pv_bf16=%d and q_on_load=%d must be 0 or 1", smooth_k, pv_bf16,
-                q_on_load);
+  if ((smooth_q != 0 && smooth_q != 1) || (smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1) ||
+      (q_on_load != 0 && q_on_load != 1))
+    return fail(ATTN_ERR_INVALID_ARG, "smooth_q=%d, smooth_k=%d, pv_bf16=%d and q_on_load=%d must be 0 or 1",
+                smooth_q, smooth_k, pv_bf16, q_on_load);
+  if (smooth_q && q_on_load)
+    return fail(ATTN_ERR_UNSUPPORTED, "smooth_q with q_on_load: the forward codes Q without block means");
   const int64_t S_pad = sage_padded_len(S);
   sa::PrepareArgs a;
   TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
@@ -586,6 +624,8 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
   a.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
   a.skip_q = q_on_load != 0;  // else the forward codes Q as it loads it
   a.skip_v = pv_bf16 != 0;
+  // Q smoothing: the means go to the workspace; the FP16 Q operand already carries them
+  if (smooth_q) a.q_mean16 = ws + L.q_mean;
   if (!pv_bf16) {
     a.v_fp8 = ws + L.v_fp8;
     a.v_scale = reinterpret_cast<float*>(ws + L.v_scale);

@@ -107,8 +107,13 @@ struct PrepareArgs {
   void* k16 = nullptr;
   bool skip_v = false;       // V not prepared (the 16-bit P V mode reads the BF16 input)
   bool skip_q = false;       // Q not prepared (the forward quantises Q as it loads it)
+  void* q_mean16 = nullptr;  // Q smoothing: output, binary16 [B*H, S_pad/32, 128] block means in step units
+                             // (nullptr: no Q smoothing); the FP16 codes (q16) are then f16(code + mean)
 };
 cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
+// Q's score operand with Q smoothing, f16(code + mean), from the INT8 codes and the block means.
+cudaError_t launch_widen_q_mean(const int8_t* q8, const void* qmean16, void* q16, long long n_codes, int num_sms,
+                               cudaStream_t stream);
 
 // Device address, in the current context, of the static scratch used by the
 // allocation-free prepare entry point; it holds kNoAllocMaxHeads * 128 words.

@@ -57,6 +57,7 @@ struct QKParams {
   float c_log2;                     // fl32(softmax_scale * log2 e), folded into Q's scales
   uint32_t* vmax;                   // [B*H*128] float bits of the channel maxima of |V|
   const float* kmean;               // [B*H*128] K smoothing: subtracted from K before quantising (or nullptr)
+  __half* qmean16;                  // [B*H, S_pad/32, 128] Q smoothing: block means in step units (or nullptr)
   int task0;                        // task of grid.z = 0 (1 when Q is skipped)
 };
 
@@ -172,7 +173,32 @@ __device__ __forceinline__ void block_coords(int warp, int& bh, int& blk) {
   blk = (int)blockIdx.x * 8 + warp;
 }
 
-__global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) {
+// The block's per-channel sums in the fixed order of the smoothing means: lane (g, L) adds
+// its rows 32j + 4t + g over t = 0..7 (rows >= S hold +0, which changes nothing), then
+//   B = (P_0 + P_1) + (P_2 + P_3)
+// by two xor shuffles; every lane of channel group L ends with the block sums of its 16
+// channels.
+__device__ __forceinline__ void block_sums16(const uint32_t (&x)[8][8], float (&acc)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int step = 0; step < 8; ++step) {
+    float f[16];
+    unpack16(x[step], f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 8));    // P_g + P_(g^1)
+    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 16));   // + the other pair
+  }
+}
+
+// kQSmooth: the instance that smooths Q (its block mean, binary16 mean output), with room
+// for the extra registers; the plain instance keeps two CTAs per SM
+template <bool kQSmooth>
+__global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(const QKParams p) {
   const int task = blockIdx.z + p.task0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int bh, blk;
@@ -226,13 +252,23 @@ __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) 
   uint32_t x[8][8];
   load_rows(p, task, bh, blk, lane, x);
 
-  // ---------------------------------------------------------- K smoothing (optional)
-  // the value quantised is fl32(k - mean[channel]); it is formed again, bit for
-  // bit, for the codes below
+  // ---------------------------------------------------------- K or Q smoothing (optional)
+  // the value quantised is fl32(x - mean[channel]); it is formed again, bit for bit, for
+  // the codes below.  K: the sequence mean from the smoothing kernels; Q: this block's own
+  // mean, block sum / valid rows
   float mu[16];
-  const bool smooth = (task == 1 && p.kmean != nullptr);
+  const bool qsmooth = kQSmooth && task == 0;
+  const bool smooth = (task == 1 && p.kmean != nullptr) || qsmooth;
+  if (qsmooth) {
+    block_sums16(x, mu);
+    // valid rows; a block wholly past S has a zero sum and gets the mean +0
+    const float n = (float)max(1, min(32, p.S - 32 * blk));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) mu[i] = smooth ? __ldg(p.kmean + (long long)bh * 128 + 16 * L + i) : 0.0f;
+    for (int i = 0; i < 16; ++i) mu[i] = __fdiv_rn(mu[i], n);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mu[i] = smooth ? __ldg(p.kmean + (long long)bh * 128 + 16 * L + i) : 0.0f;
+  }
 
   // ---------------------------------------------------------- block maximum and INT8 codes
   float a = 0.0f;
@@ -258,7 +294,37 @@ __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) 
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
-  const float inv = code_factor(a);
+  float inv;
+  uint32_t m16[8];   // Q smoothing: the block mean in step units, binary16 pairs
+  if (qsmooth) {
+    // the step is at least max |mean| / (256 * 127), so that the mean in step units fits
+    // binary16; a block whose 127 / a_eff overflows (below 127/FLT_MAX) is stored as zeros
+    float cm = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) cm = fmaxf(cm, fabsf(mu[i]));
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, d));
+    a = fmaxf(a, __fmul_rn(cm, 1.0f / 256.0f));
+    inv = code_factor(a);
+    if (isinf(inv)) {
+      inv = 0.0f;
+      a = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mu[i] = 0.0f;   // stored as zeros: +0 means, not -0
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __half2 h = __floats2half2_rn(__fmul_rn(mu[2 * i], inv), __fmul_rn(mu[2 * i + 1], inv));
+      m16[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    if (g == 0) {
+      uint4* dq = reinterpret_cast<uint4*>(p.qmean16 + ((long long)bh * p.nblk + blk) * 128 + 16 * L);
+      dq[0] = make_uint4(m16[0], m16[1], m16[2], m16[3]);
+      dq[1] = make_uint4(m16[4], m16[5], m16[6], m16[7]);
+    }
+  } else {
+    inv = code_factor(a);
+  }
   int8_t* out = p.codes[task] + ((long long)bh * p.S_pad) * 128 + 16 * L;
   __half* out16 = p.codes16[task] ? p.codes16[task] + ((long long)bh * p.S_pad) * 128 + 16 * L : nullptr;
   // codes by code_magic; its clamp only where 127 / a overflowed, a warp-uniform choice (the
@@ -277,11 +343,19 @@ __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) 
         }
       };
       if (out16) {
-        // the same codes as FP16, exact: the operand the attention kernel's Q K^T MMA reads
+        // the same codes as FP16, exact: the operand the attention kernel's Q K^T MMA reads;
+        // with Q smoothing, f16(code + mean) (one correctly rounded binary16 addition), which
+        // carries the correction term mean . k into the same product
         uint32_t hw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
           hw[i] = codes_fp16x2(code(bf_lo(x[step][i]), 2 * i), code(bf_hi(x[step][i]), 2 * i + 1));
+          if (qsmooth) {
+            const __half2 sum = __hadd2(*reinterpret_cast<const __half2*>(&hw[i]),
+                                        *reinterpret_cast<const __half2*>(&m16[i]));
+            hw[i] = *reinterpret_cast<const uint32_t*>(&sum);
+          }
+        }
         uint4* d = reinterpret_cast<uint4*>(out16 + (long long)s * 128);
         d[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         d[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
@@ -305,6 +379,39 @@ __global__ void __launch_bounds__(256, 2) prep_qk_vmax_kernel(const QKParams p) 
   if (lane == 0) p.scales[task][(long long)bh * p.nblk + blk] = block_scale(a, p.c_log2, task == 0);
 }
 
+// Q smoothing on the two-call path: Q's score operand f16(code + mean[block]) from the
+// INT8 codes and the binary16 block means, 16 elements per thread and iteration (the
+// rows of one head are consecutive, so global row / 32 is the block's index in qmean16).
+__global__ void __launch_bounds__(256) widen_q_mean_kernel(const int8_t* __restrict__ q8,
+                                                           const __half* __restrict__ qmean16,
+                                                           __half* __restrict__ q16, long long n16) {
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152, 1152
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(q8) + i);
+    const long long e0 = 16 * i;                       // first element: row e0 / 128, channel e0 % 128
+    const uint4* m4 = reinterpret_cast<const uint4*>(qmean16 + (e0 / 128 / 32) * 128 + (e0 % 128));
+    const uint4 ma = __ldg(m4), mb = __ldg(m4 + 1);
+    const uint32_t mw[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+    const uint32_t in[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    uint32_t out[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      // a byte u = code + 128 as the FP16 pattern 0x6400 | u is 1024 + u: minus 1152 is the code
+      uint32_t lo = __byte_perm(in[t], 0x64646464u, 0x5140);
+      uint32_t hi = __byte_perm(in[t], 0x64646464u, 0x7362);
+      const __half2 hl = __hadd2(__hsub2(*reinterpret_cast<__half2*>(&lo), bias),
+                                 *reinterpret_cast<const __half2*>(&mw[2 * t]));
+      const __half2 hh = __hadd2(__hsub2(*reinterpret_cast<__half2*>(&hi), bias),
+                                 *reinterpret_cast<const __half2*>(&mw[2 * t + 1]));
+      out[2 * t] = *reinterpret_cast<const uint32_t*>(&hl);
+      out[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    uint4* d = reinterpret_cast<uint4*>(q16) + 2 * i;
+    d[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
 // ------------------------------------------------------------------ K smoothing
 // mean[b, h, c] = (sum over s < S of K[b, s, h, c]) / S, K after the optional
 // RMSNorm + RoPE, in a fixed binary32 order so that the mean (which decides
@@ -326,20 +433,7 @@ __global__ void __launch_bounds__(256) prep_kmean_partial_kernel(const QKParams 
   uint32_t x[8][8];
   load_rows(p, 1, bh, blk, lane, x);
   float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#pragma unroll
-  for (int step = 0; step < 8; ++step) {
-    float f[16];
-    unpack16(x[step], f);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 8));    // P_g + P_(g^1)
-    acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xffffffffu, acc[i], 16));   // + the other pair
-  }
+  block_sums16(x, acc);
   if (g == 0) {
     float4* dst = reinterpret_cast<float4*>(partial + ((long long)bh * p.nblk + blk) * 128 + 16 * L);
 #pragma unroll
@@ -484,6 +578,7 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   p.c_log2 = a.c_log2;
   p.vmax = a.vmax;
   p.kmean = a.k_mean;
+  p.qmean16 = reinterpret_cast<__half*>(a.q_mean16);
   p.task0 = a.skip_q ? 1 : 0;
   // heads along grid.y (at most 65535 per launch, which the caller below guarantees)
   const int BH = a.B * a.H;
@@ -498,7 +593,10 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   }
   // tasks [task0, 3 or 2) over grid.z
   dim3 g1((nblk + 7) / 8, BH, (a.skip_v ? 2 : 3) - p.task0);
-  prep_qk_vmax_kernel<<<g1, 256, 0, stream>>>(p);
+  if (p.qmean16 != nullptr && p.task0 == 0)
+    prep_qk_vmax_kernel<true><<<g1, 256, 0, stream>>>(p);
+  else
+    prep_qk_vmax_kernel<false><<<g1, 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.skip_v) return cudaSuccess;
@@ -548,10 +646,23 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream) {
     c.vmax = static_cast<uint32_t*>(bytes(a.vmax, h0 * 128 * 4));
     c.k_mean = static_cast<float*>(bytes(a.k_mean, h0 * 128 * 4));
     c.k_partial = static_cast<float*>(bytes(a.k_partial, h0 * nblk * 128 * 4));
+    c.q_mean16 = bytes(a.q_mean16, h0 * nblk * 128 * 2);
     cudaError_t e = launch_prepare_heads(c, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_widen_q_mean(const int8_t* q8, const void* qmean16, void* q16, long long n_codes, int num_sms,
+                               cudaStream_t stream) {
+  const long long n16 = n_codes / 16;
+  long long blocks = (n16 + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  widen_q_mean_kernel<<<(unsigned)blocks, 256, 0, stream>>>(q8, reinterpret_cast<const __half*>(qmean16),
+                                                             reinterpret_cast<__half*>(q16), n16);
+  return cudaGetLastError();
 }
 
 }  // namespace sa

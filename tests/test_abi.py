@@ -145,23 +145,50 @@ def test_sage_attention_one_call_rejects_bad_arguments():
     L = sa.lib()
     st = I64x3(256 * 2 * 128, 256, 128)
     ws = L.sage_attention_workspace_size(1, 2, 256, 0, 0, 0)
-    # FP16 Q and K codes, their scales, e4m3 V^T, V scales and channel maxima, 256-byte pieces
-    assert ws == 2 * (2 * 256 * 128 * 2) + 2 * 256 + 2 * 128 * 256 + 1024 + 1024
-    # Q coded inside the forward: no Q codes or scales
-    assert L.sage_attention_workspace_size(1, 2, 256, 0, 0, 1) == ws - (2 * 256 * 128 * 2) - 256
+    # FP16 Q and K codes, their scales, Q's block means (Q smoothing), e4m3 V^T, V scales and
+    # channel maxima, 256-byte pieces
+    qmean = 2 * (256 // 32) * 128 * 2
+    assert ws == 2 * (2 * 256 * 128 * 2) + 2 * 256 + qmean + 2 * 128 * 256 + 1024 + 1024
+    # Q coded inside the forward: no Q codes, scales or means
+    assert L.sage_attention_workspace_size(1, 2, 256, 0, 0, 1) == ws - (2 * 256 * 128 * 2) - 256 - qmean
     assert L.sage_attention_workspace_size(1, 2, 256, 0, 1, 0) < ws       # no V in the 16-bit mode
     assert L.sage_attention_workspace_size(1, 2, 256, 1, 0, 0) > ws       # K smoothing adds its sums
 
-    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256, qload=0):
+    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256, qload=0, smooth_q=0):
         return L.sage_attention(FAKE, FAKE, FAKE, 1, S, 2, 128, st, st, st, 0.088, None, None, 1e-6, None, None, 0,
-                                smooth, pv, qload, o, st, FAKE, ws_bytes, None)
+                                smooth_q, smooth, pv, qload, o, st, FAKE, ws_bytes, None)
 
     assert call(smooth=2) == 1
+    assert call(smooth_q=2) == 1
+    assert call(smooth_q=1, qload=1) == 3       # Q coded on load has no block means
     assert call(pv=-1) == 1
     assert call(qload=3) == 1
     assert call(o=FAKE + 2) == 2
     assert call(ws_bytes=ws - 1) == 1
     assert call(S=0) == 1
+
+
+def test_smoothed_prepare_and_forward_reject_bad_arguments():
+    L = sa.lib()
+    st = I64x3(256 * 2 * 128, 256, 128)
+
+    def prep(smooth_q=1, smooth_k=0, q_mean=FAKE, k_mean=FAKE):
+        return L.sage_prepare_smoothed(FAKE, FAKE, FAKE, 1, 256, 2, 128, st, st, st, 0.088, None, None, 1e-6, None,
+                                       None, 0, 256, smooth_q, smooth_k, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, q_mean,
+                                       k_mean, FAKE, 1 << 20, None)
+
+    assert prep(smooth_q=2) == 1
+    assert prep(smooth_k=-1) == 1
+    assert prep(q_mean=None) == 1
+    assert prep(q_mean=FAKE + 4) == 2
+    assert prep(smooth_q=0, smooth_k=1, k_mean=None) == 1
+    ws = L.sage_attn_workspace_size(1, 2, 256)
+    assert L.sage_attn_fwd_smooth_q(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 128, 256, FAKE, ws,
+                                    None) == 1
+    assert L.sage_attn_fwd_smooth_q(FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, st, 1, 256, 2, 128, 256, FAKE,
+                                    ws, None) == 2
+    assert L.sage_attn_fwd_pv16_smooth_q(FAKE, None, FAKE, FAKE, FAKE, FAKE, st, FAKE, st, 1, 256, 2, 128, 256, FAKE,
+                                         ws, None) == 1
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -50,6 +50,7 @@ class Workload:
     S: int
     seed: int
     k_channel_offset_std: float = 0.0   # flux1024: per-(head, channel) K mean offset
+    q_channel_offset_std: float = 0.0   # Q smoothing cases: per-(head, channel) Q mean offset
     outlier_frac: float = 0.0           # wan720p: fraction of tokens scaled
     outlier_gain: float = 1.0
     head_major_storage: bool = False    # hunyuan720p: [B,H,S,D] storage
@@ -160,6 +161,12 @@ def make_inputs(wl: Workload, device="cpu") -> Inputs:
         for t in (q, k, v):
             # [B, S, H, D] layout here (outliers are not combined with head-major storage)
             t[:, tok] = t[:, tok] * gain
+    if wl.q_channel_offset_std > 0:
+        # drawn after everything else, so that the other tensors match the recipe without it
+        mu = torch.randn((H, D), generator=g, device=device, dtype=torch.float32) * wl.q_channel_offset_std
+        mu = mu[None, :, None, :] if wl.head_major_storage else mu[None, None, :, :]
+        q = (q.float() + mu).to(torch.bfloat16)
+        inp.q = q
     if wl.head_major_storage:
         inp.q = q.permute(0, 2, 1, 3)
         inp.k = k.permute(0, 2, 1, 3)
