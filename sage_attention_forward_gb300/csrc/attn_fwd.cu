@@ -292,6 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
+  // nothing above reads what an earlier kernel in the stream writes; launched as a
+  // programmatic dependent (after the prepare or the widening pass) the kernel gets this
+  // far while that kernel finishes, and waits here before its first such read
+  griddep_wait();
   if constexpr (kMode == Mode::kSageFP8) {
     // staged once: every epilogue thread reads all 128, which from global memory would cost
     // a round of load latency per 32-column chunk at the end of every CTA
@@ -733,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) widen_i8_f16_kernel(const int8_t* __restrict__ q8, const int8_t* __restrict__ k8,
                                                           __half* __restrict__ q16, __half* __restrict__ k16,
                                                           long long n16) {
+  griddep_launch_dependents();   // the attention kernel may set up meanwhile (it waits for this grid)
   const int8_t* src = blockIdx.y == 0 ? q8 : k8;
   __half* dst = blockIdx.y == 0 ? q16 : k16;
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152, 1152
@@ -805,8 +810,18 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   // along grid.y, and grid.z when there are more than 65535 of them
   const unsigned ny = (unsigned)(p.BH < 65535 ? p.BH : 65535);
   dim3 grid((S + kNQ * kBM - 1) / (kNQ * kBM), ny, (p.BH + ny - 1) / ny);
-  attn_fwd_kernel<kMode, kQLoad><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel in the stream (see griddep_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<kMode, kQLoad>, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace

@@ -126,6 +126,16 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ----------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start while the previous kernel in its stream is still running, once every CTA of
+// that kernel has executed launch_dependents (or exited).  Before it reads anything the
+// previous kernel writes it must wait: griddep_wait returns when that kernel has
+// completed and its memory operations are visible.  In a kernel launched without the
+// attribute the wait returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

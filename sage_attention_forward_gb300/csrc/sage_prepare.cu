@@ -199,6 +199,7 @@ __device__ __forceinline__ void block_sums16(const uint32_t (&x)[8][8], float (&
 // for the extra registers; the plain instance keeps two CTAs per SM
 template <bool kQSmooth>
 __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(const QKParams p) {
+  griddep_launch_dependents();   // the next kernel may set up meanwhile (it waits for this grid)
   const int task = blockIdx.z + p.task0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int bh, blk;
@@ -477,6 +478,8 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
 
 // blockIdx.x = 128-position tile, blockIdx.y = head b * H + h
 __global__ void __launch_bounds__(128) prep_v_kernel(const VParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // the channel maxima come from prep_qk_vmax_kernel
   const int bh = (int)blockIdx.y;
   const int tile = (int)blockIdx.x;
   const int b = bh / p.H, h = bh % p.H;
@@ -614,8 +617,17 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   vp.codes = a.v_fp8;
   vp.scales = a.v_scale;
   dim3 g2((unsigned)(a.S_pad / 128), BH, 1);
-  prep_v_kernel<<<g2, 128, 0, stream>>>(vp);
-  return cudaGetLastError();
+  // a programmatic dependent of prep_qk_vmax_kernel (it waits before reading the maxima)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = g2;
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prep_v_kernel, vp);
 }
 
 }  // namespace
