@@ -307,6 +307,7 @@ def run_ours(args, rank, world):
     ws_s = sa.prepare_workspace(B, H, dev, S_pad, smooth_k=True)
     ws_16 = sa.sage_attention_workspace(B, H, S, dev, pv="bf16")
     ws_ql = sa.sage_attention_workspace(B, H, S, dev, q_on_load=True)
+    ws_kl = sa.sage_attention_workspace(B, H, S, dev, q_on_load=True, k_on_load=True)
     sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p, **kw)
     calls = {
         "bf16": lambda: sa.attn_fwd_bf16(q, k, v, out=o_bf16, softmax_scale=scale),
@@ -318,6 +319,8 @@ def run_ours(args, rank, world):
                                                **kw),
         "sage_q_on_load": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_pv16, workspace=ws_ql,
                                                     q_on_load=True, **kw),
+        "sage_qk_on_load": lambda: sa.sage_attention(q, k, v, softmax_scale=scale, out=o_pv16, workspace=ws_kl,
+                                                     k_on_load=True, **kw),
         "sage_core": lambda: sa.sage_attn_fwd(prep, out=o_sage, workspace=ws_a),
         "sage_pv16_core": lambda: sa.sage_attn_fwd_pv16(prep, v, out=o_pv16, workspace=ws_a),
         "prepare": lambda: sa.sage_prepare(q, k, v, softmax_scale=scale, S_pad=S_pad, out=prep, workspace=ws_p,
@@ -352,6 +355,8 @@ def run_ours(args, rank, world):
         "sage_two_calls": attn_entry("sage_two_calls", None, "sage_prepare, then sage_attn_fwd"),
         "sage_pv16": attn_entry("sage_pv16", None, "sage_attention(pv=bf16)"),
         "sage_q_on_load": attn_entry("sage_q_on_load", None, "sage_attention(q_on_load=True): Q coded by the forward"),
+        "sage_qk_on_load": attn_entry("sage_qk_on_load", None,
+                                      "sage_attention(k_on_load=True): Q and K coded by the forward"),
         # Q K^T on the FP16 MMA (the kind::f16 rate), P V on the e4m3 MMA (twice that rate)
         "sage_core": attn_entry("sage_core", rate_sage),
         "sage_pv16_core": attn_entry("sage_pv16_core", rate_bf16),
@@ -371,7 +376,7 @@ def run_ours(args, rank, world):
                                 if in_step["sage"]["mcycles"] and in_step["bf16"]["mcycles"] else None),
         "note": "one-call Sage (prepare included) over BF16; below 1 means Sage is faster",
     }
-    del prep_s, ws_s, o_pv16, ws_16, ws_ql
+    del prep_s, ws_s, o_pv16, ws_16, ws_ql, ws_kl
 
     # ------------------------------------------------------------- end to end
     e2e = run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist)

@@ -375,15 +375,23 @@ ATTN_API size_t sage_attention_workspace_size(int B, int H, int64_t S_pad, int s
  *   smooth_k   : 0 or 1 -- K smoothing as sage_prepare_smooth_k
  *   pv_bf16    : 0 -- P and V in e4m3 (sage_attn_fwd); 1 -- P in BF16 times the
  *                BF16 V input (sage_attn_fwd_pv16; V is then not quantised)
- *   q_on_load  : 0 -- Q coded by the prepare; 1 -- Q coded by the forward as it
- *                is loaded
+ *   q_on_load  : 0 -- Q and K coded by the prepare; 1 -- Q coded by the forward as
+ *                it is loaded; 2 -- Q and K coded by the forward as they are loaded
+ *                (each K tile by a softmax warpgroup while its next S product runs;
+ *                the block scales stay in shared memory; with pv_bf16 = 1 no prepare
+ *                kernel runs at all).  Every CTA of a head then codes all of the
+ *                head's K tiles, so on a GB300 level 2 measured slower at every size
+ *                (3x at 76112 tokens); levels 1 and 2 exist for callers that must not
+ *                write codes to memory.  Not with smooth_q (1, 2) or smooth_k (2):
+ *                ATTN_ERR_UNSUPPORTED
  *   o, o_str   : BF16 [B, S, H, 128] output, element strides (as sage_attn_fwd)
  *   workspace  : at least sage_attention_workspace_size(B, H, sage_padded_len(S),
  *                smooth_k, pv_bf16, q_on_load) bytes, 16-byte aligned; contents
- *                on entry do not matter.
+ *                on entry do not matter.  May be NULL when that size is 0
+ *                (pv_bf16 = 1 with q_on_load = 2: nothing is prepared).
  * Enqueues the prepare kernels (one to four) and the attention kernel on
- * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_q, smooth_k,
- * pv_bf16 or q_on_load other than 0/1 -> ATTN_ERR_INVALID_ARG.
+ * `stream`.  Errors as sage_prepare and sage_attn_fwd; smooth_q, smooth_k or
+ * pv_bf16 other than 0/1, q_on_load other than 0/1/2 -> ATTN_ERR_INVALID_ARG.
  */
 ATTN_API attn_status sage_attention(const void* q, const void* k, const void* v, int B, int S, int H, int D,
                                     const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],

@@ -346,23 +346,31 @@ def sage_attn_fwd_pv16(prep: Prepared, v: torch.Tensor, out: torch.Tensor | None
     return out
 
 
+def _on_load_level(q_on_load: bool, k_on_load: bool) -> int:
+    """0: the prepare codes Q and K; 1: the forward codes Q; 2: the forward codes Q and K."""
+    return 2 if k_on_load else int(bool(q_on_load))
+
+
 def sage_attention_workspace(B: int, H: int, S: int, device, smooth_k: bool = False, pv: str = "e4m3",
-                             q_on_load: bool = False) -> torch.Tensor:
+                             q_on_load: bool = False, k_on_load: bool = False) -> torch.Tensor:
     n = int(lib().sage_attention_workspace_size(B, H, sage_padded_len(S), int(smooth_k), int(pv == "bf16"),
-                                                int(bool(q_on_load))))
+                                                _on_load_level(q_on_load, k_on_load)))
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rms_eps=1e-6, rope_cos=None,
                    rope_sin=None, rope_dim=0, out=None, stream=None, smooth_k=False, pv="e4m3",
-                   workspace=None, q_on_load=False, smooth_q=False) -> torch.Tensor:
+                   workspace=None, q_on_load=False, smooth_q=False, k_on_load=False) -> torch.Tensor:
     """Prepare + attention in one library call: the SageAttention-style forward of BF16 Q/K/V.
 
     pv="e4m3": P and V in FP8; pv="bf16": P in BF16 times the unquantised V.  The
     prepared tensors stay in `workspace` (allocated here unless given).  q_on_load:
     Q is coded by the forward as it loads it instead of by the prepare (the same
-    output; slower on a GB300).  smooth_q / smooth_k: block-mean smoothing of Q
-    (with its correction term) / sequence-mean smoothing of K before INT8."""
+    output; slower on a GB300).  k_on_load: the forward codes K (and Q) too, per tile,
+    so neither reaches memory as codes (with pv="bf16" nothing is prepared at all);
+    every CTA of a head then codes all its K tiles, which is slower at every size.
+    smooth_q / smooth_k: block-mean smoothing of Q (with its correction term) /
+    sequence-mean smoothing of K before INT8."""
     if pv not in ("e4m3", "bf16"):
         raise ValueError(f"pv must be 'e4m3' or 'bf16', not {pv!r}")
     B, S, H, D = q.shape
@@ -371,7 +379,7 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
     if out is None:
         out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=q.device)
     if workspace is None:
-        workspace = sage_attention_workspace(B, H, S, q.device, smooth_k, pv, q_on_load)
+        workspace = sage_attention_workspace(B, H, S, q.device, smooth_k, pv, q_on_load, k_on_load)
     qs, ks, vs, os_ = _bshd("q", q), _bshd("k", k), _bshd("v", v), _bshd("out", out)
 
     def ptr(t):
@@ -380,7 +388,8 @@ def sage_attention(q, k, v, softmax_scale=None, q_norm_w=None, k_norm_w=None, rm
     _check(lib().sage_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, H, D, qs, ks, vs,
                                 float(softmax_scale), ptr(q_norm_w), ptr(k_norm_w), float(rms_eps), ptr(rope_cos),
                                 ptr(rope_sin), int(rope_dim), int(bool(smooth_q)), int(bool(smooth_k)), int(pv == "bf16"),
-                                int(bool(q_on_load)), out.data_ptr(), os_, workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)))
+                                _on_load_level(q_on_load, k_on_load), out.data_ptr(), os_, workspace.data_ptr(),
+                                workspace.numel(), _stream_ptr(stream)))
     return out
 
 

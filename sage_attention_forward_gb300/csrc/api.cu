@@ -567,8 +567,10 @@ static FusedLayout fused_layout(int B, int H, int64_t S_pad, int smooth_k, int p
     L.q_scale = take(bh * nblk * 4);
     L.q_mean = take(bh * nblk * 128 * 2);   // used with Q smoothing only
   }
-  L.k16 = take(bh * (size_t)S_pad * 128 * 2);
-  L.k_scale = take(bh * nblk * 4);
+  if (q_on_load < 2) {
+    L.k16 = take(bh * (size_t)S_pad * 128 * 2);
+    L.k_scale = take(bh * nblk * 4);
+  }
   if (!pv_bf16) {
     L.v_fp8 = take(bh * 128 * (size_t)S_pad);
     L.v_scale = take(bh * 128 * 4);
@@ -597,20 +599,23 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
   TRY(check_shape(B, S, H, D, &empty));
   if (empty) return ATTN_OK;
   if ((smooth_q != 0 && smooth_q != 1) || (smooth_k != 0 && smooth_k != 1) || (pv_bf16 != 0 && pv_bf16 != 1) ||
-      (q_on_load != 0 && q_on_load != 1))
-    return fail(ATTN_ERR_INVALID_ARG, "smooth_q=%d, smooth_k=%d, pv_bf16=%d and q_on_load=%d must be 0 or 1",
+      q_on_load < 0 || q_on_load > 2)
+    return fail(ATTN_ERR_INVALID_ARG, "smooth_q=%d, smooth_k=%d and pv_bf16=%d must be 0 or 1, q_on_load=%d 0, 1 or 2",
                 smooth_q, smooth_k, pv_bf16, q_on_load);
   if (smooth_q && q_on_load)
     return fail(ATTN_ERR_UNSUPPORTED, "smooth_q with q_on_load: the forward codes Q without block means");
+  if (smooth_k && q_on_load == 2)
+    return fail(ATTN_ERR_UNSUPPORTED, "smooth_k with K coded on load: the sequence mean of K needs its own pass");
   const int64_t S_pad = sage_padded_len(S);
   sa::PrepareArgs a;
   TRY(prepare_inputs(q, k, v, B, S, H, q_str, k_str, v_str, softmax_scale, q_norm_w, k_norm_w, rms_eps, rope_cos,
                      rope_sin, rope_dim, S_pad, a));
   long long os[3];
   TRY(check_strides("o", o, o_str, B, S, H, os));
-  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
-  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   const FusedLayout L = fused_layout(B, H, S_pad, smooth_k, pv_bf16, q_on_load);
+  // with the 16-bit P V and Q and K coded on load nothing is prepared: no workspace at all
+  if (L.total > 0 && !workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   if (workspace_bytes < L.total)
     return fail(ATTN_ERR_INVALID_ARG, "sage_attention: workspace_bytes=%zu < %zu required", workspace_bytes, L.total);
   TRY(check_device());
@@ -620,9 +625,12 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
     a.q16 = ws + L.q16;
     a.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
   }
-  a.k16 = ws + L.k16;
-  a.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
+  if (q_on_load < 2) {
+    a.k16 = ws + L.k16;
+    a.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
+  }
   a.skip_q = q_on_load != 0;  // else the forward codes Q as it loads it
+  a.skip_k = q_on_load == 2;  // ... and K
   a.skip_v = pv_bf16 != 0;
   // Q smoothing: the means go to the workspace; the FP16 Q operand already carries them
   if (smooth_q) a.q_mean16 = ws + L.q_mean;
@@ -635,10 +643,34 @@ attn_status sage_attention(const void* q, const void* k, const void* v, int B, i
     a.k_mean = reinterpret_cast<float*>(ws + L.k_mean);
     a.k_partial = reinterpret_cast<float*>(ws + L.k_partial);
   }
-  cudaError_t e = sa::launch_sage_prepare(a, (cudaStream_t)stream);
+  // (nothing to prepare when the forward codes Q and K and V stays in BF16)
+  cudaError_t e = (q_on_load == 2 && pv_bf16) ? cudaSuccess : sa::launch_sage_prepare(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "sage_attention prepare");
   const long long bh = (long long)B * H;
   CUtensorMap tq, tk, tv;
+  if (q_on_load == 2) {
+    // Q and K are coded by the forward: both through their BF16 [B, S, H, 128] maps
+    TRY(tmap_bhsd_bf16(&tq, q, B, S, H, a.str[0]));
+    TRY(tmap_bhsd_bf16(&tk, k, B, S, H, a.str[1]));
+    sa::QLoadArgs qa;
+    qa.q_norm_w = a.q_norm_w;
+    qa.k_norm_w = a.k_norm_w;
+    qa.rms_eps = a.rms_eps;
+    qa.rope_cos = a.rope_cos;
+    qa.rope_sin = a.rope_sin;
+    qa.rope_dim = a.rope_dim;
+    qa.c_log2 = a.c_log2;
+    if (pv_bf16) {
+      TRY(tmap_bhsd_bf16(&tv, v, B, S, H, a.str[2]));
+      e = sa::launch_sage_attn_pv16_qkload(tq, tk, tv, qa, o, os[0], os[1], os[2], B, S, H, S_pad, (cudaStream_t)stream);
+    } else {
+      TRY(tmap_bytes_3d(&tv, a.v_fp8, S_pad, 128, bh));
+      e = sa::launch_sage_attn_qkload(tq, tk, tv, qa, a.v_scale, o, os[0], os[1], os[2], B, S, H, S_pad,
+                                      (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "sage_attention launch");
+    return ATTN_OK;
+  }
   TRY(tmap_f16_rows(&tk, a.k16, S_pad, bh));
   if (!q_on_load) {
     TRY(tmap_f16_rows(&tq, a.q16, S_pad, bh));

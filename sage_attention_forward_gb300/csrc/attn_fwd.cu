@@ -56,6 +56,7 @@
 // block, whose maximum is a warp reduction.  Each thread then makes its writes
 // visible to the tensor core's proxy and arrives on q_ready[i], which the MMA
 // warp waits on before Q_i's first product.  Q then never reaches HBM as codes.
+#include <cstddef>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -118,10 +119,22 @@ struct __align__(1024) Smem {
   uint64_t o_done[kNQ];
   uint64_t mma_drain;
   uint64_t q_ready[kNQ];     // quantise-on-load: all 128 rows of Q_i coded in place
-  float v_scale[128];        // FP8 mode: the head's V channel scales, for the epilogue
+  // K coded on load: tile t coded in place (128 threads), a ring by t % 4 rather than by K slot.
+  // Indexed by slot, with two slots, a phase could be completed twice before the warpgroup that
+  // only reads tile t's scales waited on it (tiles t and t + 2 are coded by the other warpgroup
+  // while the reader is busy coding t + 1) and that wait would then target tile t + 4's phase,
+  // which needs the reader's own progress.  Tile t + 4 is coded only after both warpgroups have
+  // published P(t + 1), so no wait on tile t's phase can be overtaken.
+  uint64_t k_coded[4];
+  // read as float4 / float2: the barriers above are an odd count of 8-byte words in some modes
+  alignas(16) float ks[4][4];         // K coded on load: the 32-key block scales of K tile t in ks[t % 4]
+  alignas(16) float v_scale[128];     // FP8 mode: the head's V channel scales, for the epilogue
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+static_assert(offsetof(Smem<Mode::kSageFP8>, ks) % 16 == 0 && offsetof(Smem<Mode::kSagePV16>, ks) % 16 == 0 &&
+                  offsetof(Smem<Mode::kSageFP8>, v_scale) % 16 == 0,
+              "the scale arrays are read as vectors");
 
 __device__ uint32_t g_err_attn;
 
@@ -140,6 +153,7 @@ struct Params {
   int withhold_loads;     // self-test of the failure path: the producer loads nothing
   // quantise-on-load of Q
   const __nv_bfloat16* q_norm_w;   // [128] or nullptr
+  const __nv_bfloat16* k_norm_w;   // [128] or nullptr (K coded on load)
   float rms_eps;
   const __nv_bfloat16* rope_cos;   // [S, rope_dim] or nullptr
   const __nv_bfloat16* rope_sin;
@@ -175,11 +189,13 @@ __device__ __forceinline__ void rope_row(uint32_t (&x)[64], const __nv_bfloat16*
   }
 }
 
-// Quantise-on-load: the calling thread's row `row` of a BF16 Q tile (two [128][64]
-// halves, 128-byte swizzle) becomes its FP16 codes in place; returns the row's score
-// factor (its 32-row block's scale, softmax_scale * log2 e included).  The whole warp
-// calls it: its 32 rows are one block.  grow = the row's position in the sequence.
-__device__ __noinline__ float quantise_q_row(uint8_t* qtile, int row, int grow, const Params& p, float c_log2) {
+// Quantise-on-load: the calling thread's row `row` of a BF16 Q or K tile (two [128][64]
+// halves, 128-byte swizzle) becomes its FP16 codes in place (RMSNorm with norm_w when
+// given, then RoPE, as the prepare does); returns its 32-row block's scale, times mult
+// for Q (softmax_scale * log2 e).  The whole warp calls it: its 32 rows are one block.
+// grow = the row's position in the sequence.
+__device__ __noinline__ float quantise_row(uint8_t* qtile, int row, int grow, const Params& p,
+                                           const __nv_bfloat16* norm_w, float mult, bool is_q) {
   uint32_t x[64];
   uint8_t* const rp = qtile + row * 128;   // the row in the first half; the second is kHalfBytes on
 #pragma unroll
@@ -192,12 +208,12 @@ __device__ __noinline__ float quantise_q_row(uint8_t* qtile, int row, int grow, 
       x[32 * hf + 4 * c + 2] = v.z;
       x[32 * hf + 4 * c + 3] = v.w;
     }
-  if (p.q_norm_w != nullptr) {
+  if (norm_w != nullptr) {
     float P[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) P[g] = qk::sumsq16(&x[8 * g]);
     const float r = qk::rms_factor(qk::sumsq_combine(P), p.rms_eps);
-    const uint4* w4 = reinterpret_cast<const uint4*>(p.q_norm_w);
+    const uint4* w4 = reinterpret_cast<const uint4*>(norm_w);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const uint4 w = __ldg(w4 + c);
@@ -242,10 +258,86 @@ __device__ __noinline__ float quantise_q_row(uint8_t* qtile, int row, int grow, 
     for (int c = 0; c < 8; ++c)
       *reinterpret_cast<uint4*>(rp + hf * kHalfBytes + ((c ^ (row & 7)) << 4)) =
           make_uint4(x[32 * hf + 4 * c], x[32 * hf + 4 * c + 1], x[32 * hf + 4 * c + 2], x[32 * hf + 4 * c + 3]);
-  return qk::block_scale(a, c_log2, true);
+  return qk::block_scale(a, mult, is_q);
 }
 
-template <Mode kMode, bool kQLoad>
+// The same coding worked in shared memory a word (two channels) or a RoPE pair of words at
+// a time, so that few registers are live: the K tiles are coded inside the softmax loop,
+// where the loop's own state must stay in registers.  Same arithmetic, same order.
+__device__ __forceinline__ float quantise_row_smem(uint8_t* qtile, int row, int grow, const Params& p,
+                                                  const __nv_bfloat16* norm_w, float mult, bool is_q) {
+  uint8_t* const rp = qtile + row * 128;   // the row in the first half; the second is kHalfBytes on
+  // word w (channels 2w, 2w + 1): half w / 32, 16-byte chunk (w % 32) / 4 swizzled by the row
+  auto word = [&](int w) -> uint32_t* {
+    return reinterpret_cast<uint32_t*>(rp + (w >> 5) * kHalfBytes + ((((w & 31) >> 2) ^ (row & 7)) << 4) +
+                                       ((w & 3) << 2));
+  };
+  const bool norm = norm_w != nullptr;
+  const uint32_t* nw = reinterpret_cast<const uint32_t*>(norm_w);
+  float r = 0.0f;
+  if (norm) {
+    float P[8];
+#pragma unroll 1
+    for (int g = 0; g < 8; ++g) {
+      uint32_t xx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) xx[k] = *word(8 * g + k);
+      P[g] = qk::sumsq16(xx);
+    }
+    r = qk::rms_factor(qk::sumsq_combine(P), p.rms_eps);
+  }
+  uint32_t m2 = 0u;
+  if (grow >= p.S) {
+    // rows past S are zeros (with rms_eps = 0 their RMSNorm factor is infinite) and code to 0
+#pragma unroll 4
+    for (int w = 0; w < 64; ++w) *word(w) = 0u;
+  } else {
+    const int kW = p.rope_dim / 4;   // RoPE pairs words (w, w + kW), w < kW
+    const uint32_t* cs = p.rope_dim ? reinterpret_cast<const uint32_t*>(p.rope_cos + (long long)grow * p.rope_dim)
+                                    : nullptr;
+    const uint32_t* sn = p.rope_dim ? reinterpret_cast<const uint32_t*>(p.rope_sin + (long long)grow * p.rope_dim)
+                                    : nullptr;
+#pragma unroll 2
+    for (int w = 0; w < kW; ++w) {
+      uint32_t lo = *word(w), hi = *word(w + kW);
+      if (norm) {
+        lo = qk::rms_apply(lo, r, __ldg(nw + w));
+        hi = qk::rms_apply(hi, r, __ldg(nw + w + kW));
+      }
+      const uint32_t nlo = qk::rope_first_half(lo, hi, __ldg(cs + w), __ldg(sn + w));
+      const uint32_t nhi = qk::rope_second_half(hi, lo, __ldg(cs + w + kW), __ldg(sn + w + kW));
+      *word(w) = nlo;
+      *word(w + kW) = nhi;
+      m2 = qk::bf2_max(m2, qk::bf2_max(qk::bf2_abs(nlo), qk::bf2_abs(nhi)));
+    }
+#pragma unroll 4
+    for (int w = 2 * kW; w < 64; ++w) {
+      uint32_t x = *word(w);
+      if (norm) {
+        x = qk::rms_apply(x, r, __ldg(nw + w));
+        *word(w) = x;
+      }
+      m2 = qk::bf2_max(m2, qk::bf2_abs(x));
+    }
+  }
+  float a = fmaxf(qk::bf_lo(m2), qk::bf_hi(m2));
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+  const float inv = qk::code_factor(a);
+  auto emit = [&](auto kClamp) {
+    constexpr bool kC = decltype(kClamp)::value;
+#pragma unroll 4
+    for (int w = 0; w < 64; ++w) {
+      const uint32_t x = *word(w);
+      *word(w) = qk::codes_fp16x2(qk::code_magic<kC>(qk::bf_lo(x), inv), qk::code_magic<kC>(qk::bf_hi(x), inv));
+    }
+  };
+  if (isinf(inv)) emit(std::true_type{});   // warp-uniform: 127 / a overflowed
+  else emit(std::false_type{});
+  return qk::block_scale(a, mult, is_q);
+}
+
+template <Mode kMode, bool kQLoad, bool kKLoad>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -285,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sm.mma_drain, 1);
     for (int i = 0; i < kNQ; ++i) mbar_init(&sm.q_ready[i], 4 * 32);
+    for (int t = 0; t < 4; ++t) mbar_init(&sm.k_coded[t], 4 * 32);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -334,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&sm.k_full[slot], kQTileBytes);
-          if constexpr (kInt8) {
+          if constexpr (kInt8 && !kKLoad) {
             tma_load_3d(sm.k[slot], &tm_k, &sm.k_full[slot], 0, j * kBN, bh);
             tma_load_3d(sm.k[slot] + kHalfBytes, &tm_k, &sm.k_full[slot], 64, j * kBN, bh);
           } else {
@@ -429,6 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
 
+      // K_j is ready when its tile has landed, or with K coded on load when a softmax
+      // warpgroup has coded it in place
+      // (slot = t % kKStages, a compile-time constant in the unrolled loop below)
+      auto wait_k = [&](int t, int slot) -> bool {
+        if constexpr (kKLoad)
+          return mbar_wait_warp<false>(&sm.k_coded[t & 3], (t >> 2) & 1, abort_flag, err, kErrTimeoutSync);
+        else
+          return mbar_wait_warp<false>(&sm.k_full[slot], (t / kKStages) & 1, abort_flag, err, kErrTimeoutTma);
+      };
       // Q_i is ready when its tile has landed, or with quantise-on-load when its 128 softmax
       // threads have coded it in place
       auto wait_q = [&](int i) -> bool {
@@ -436,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else return i > 0 || mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
       };
       bool ok = wait_q(0);
-      if (ok) ok = mbar_wait_warp<false>(&sm.k_full[0], 0, abort_flag, err, kErrTimeoutTma);
+      if (ok) ok = wait_k(0, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -468,17 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // takes that wait off the path from P_0 V_j to S_0(j+1); with two stages it often
           // is not yet, and the wait stays where S_0 needs it
           constexpr bool kEarlyK = (kKStages >= 3);
-          if (kEarlyK && more &&
-              !mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
-                                     kErrTimeoutTma)) {
+          if (kEarlyK && more && !wait_k(j + 1, slotK)) {
             ok = false;
             break;
           }
           if (!issue_pv(0, slotV, j)) { ok = false; break; }
           if (more) {
-            if (!kEarlyK &&
-                !mbar_wait_warp<false>(&sm.k_full[slotK], ((j + 1) / kKStages) & 1, abort_flag, err,
-                                       kErrTimeoutTma)) {
+            if (!kEarlyK && !wait_k(j + 1, slotK)) {
               ok = false;
               break;
             }
@@ -512,11 +610,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // first, before the rest of the row's state exists: code the row in place
       ok = mbar_wait_warp<false>(&sm.q_full, 0, abort_flag, err, kErrTimeoutTma);
       if (ok) {
-        qs = quantise_q_row(sm.q[i], row, q_row0 + i * kBM + row, p, p.c_log2);
+        if constexpr (kKLoad)   // (the low-register coder here too: this instance's budget is the loop's)
+          qs = quantise_row_smem(sm.q[i], row, q_row0 + i * kBM + row, p, p.q_norm_w, p.c_log2, true);
+        else
+          qs = quantise_row(sm.q[i], row, q_row0 + i * kBM + row, p, p.q_norm_w, p.c_log2, true);
         // the codes are read by the tensor core (the async proxy) once all 128 rows are in
         fence_proxy_async_smem();
         mbar_arrive(&sm.q_ready[i]);
       }
+    }
+    // K coded on load: warpgroup i codes the K tiles t with t % 2 == i, K_i first and then
+    // K_{j+2} as soon as it has published P_i(j), j % 2 == i (the window until S_i(j+1) is
+    // done); its four warps take one 32-key block each, a thread one key row, with the
+    // prepare's arithmetic.  The block scales go to ks[t % 4], read by both warpgroups'
+    // softmax of tile t, and rewritten (for tile t + 4) only after both have moved on.
+    auto code_k = [&](int t) -> bool {
+      const int slot = t % kKStages;
+      if (!mbar_wait_warp<false>(&sm.k_full[slot], (t / kKStages) & 1, abort_flag, err, kErrTimeoutTma)) return false;
+      const float ksc = quantise_row_smem(sm.k[slot], row, t * kBN + row, p, p.k_norm_w, 1.0f, false);
+      if (lane == 0) sm.ks[t & 3][wq] = ksc;
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.k_coded[t & 3]);
+      return true;
+    };
+    if constexpr (kKLoad) {
+      if (ok && i < p.n_tiles) ok = code_k(i);
     }
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128u * i;
@@ -529,8 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qblk = min(grow, p.nblk * 32 - 1) >> 5;
         qs = __ldg(p.q_scale + (long long)bh * p.nblk + qblk);
       }
-      ksp = p.k_scale + (long long)bh * p.nblk;
-      ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
+      if constexpr (!kKLoad) {
+        ksp = p.k_scale + (long long)bh * p.nblk;
+        ks_next = __ldg(reinterpret_cast<const float4*>(ksp));
+      }
     }
     float m_used = -INFINITY, l = 0.0f;
 
@@ -538,13 +658,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K scales of the tile's four 32-key blocks: prefetched a tile ahead in the FP8 mode;
       // the 16-bit mode, whose BF16 P takes twice the registers, loads them when needed
       float4 ks4 = ks_next;
-      if constexpr (kFP8) {
+      if constexpr (kKLoad) {
+        // (the scales come from shared memory once the tile is coded, below)
+      } else if constexpr (kFP8) {
         if (j + 1 < n) ks_next = __ldg(reinterpret_cast<const float4*>(ksp + 4 * (j + 1)));
       } else if constexpr (kInt8) {
         ks4 = __ldg(reinterpret_cast<const float4*>(ksp + 4 * j));
       }
-      const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
       if (!mbar_wait_warp<false>(&sm.s_full[i], j & 1, abort_flag, err, kErrTimeoutMma)) { ok = false; break; }
+      if constexpr (kKLoad) {
+        // this tile's block scales, from the warpgroup that coded it
+        if (!mbar_wait_warp<false>(&sm.k_coded[j & 3], (j >> 2) & 1, abort_flag, err, kErrTimeoutSync)) {
+          ok = false;
+          break;
+        }
+        ks4 = *reinterpret_cast<const float4*>(sm.ks[j & 3]);
+      }
+      const float f[4] = {qs * ks4.x, qs * ks4.y, qs * ks4.z, qs * ks4.w};
       tc_fence_after();
       uint32_t s[128];
       uint32_t(&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
@@ -689,6 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       else p_section(std::false_type{});
       if (!ok) break;
       l += rs0 + rs1;
+      if constexpr (kKLoad) {
+        if ((j & 1) == i && j + 2 < n && !code_k(j + 2)) {
+          ok = false;
+          break;
+        }
+      }
 
     }
 
@@ -765,7 +901,7 @@ size_t smem_bytes_of() {
   return sizeof(Smem<kMode>) + 1024;
 }
 
-template <Mode kMode, bool kQLoad = false>
+template <Mode kMode, bool kQLoad = false, bool kKLoad = false>
 cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const float* q_scale, const float* k_scale, const float* v_scale, float c_log2, void* o,
                           long long o_sb, long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
@@ -775,7 +911,7 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   static ContextOnce attr_done;
   const size_t smem = smem_bytes_of<kMode>();
   cudaError_t e = attr_done.run([] {
-    return cudaFuncSetAttribute(attn_fwd_kernel<kMode, kQLoad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(attn_fwd_kernel<kMode, kQLoad, kKLoad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem_bytes_of<kMode>());
   });
   if (e != cudaSuccess) return e;
@@ -795,11 +931,13 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   p.BH = B * H;
   p.withhold_loads = withhold_loads ? 1 : 0;
   p.q_norm_w = nullptr;
+  p.k_norm_w = nullptr;
   p.rms_eps = 0.0f;
   p.rope_cos = p.rope_sin = nullptr;
   p.rope_dim = 0;
   if (qa != nullptr) {
     p.q_norm_w = reinterpret_cast<const __nv_bfloat16*>(qa->q_norm_w);
+    p.k_norm_w = reinterpret_cast<const __nv_bfloat16*>(qa->k_norm_w);
     p.rms_eps = qa->rms_eps;
     p.rope_cos = reinterpret_cast<const __nv_bfloat16*>(qa->rope_cos);
     p.rope_sin = reinterpret_cast<const __nv_bfloat16*>(qa->rope_sin);
@@ -821,7 +959,7 @@ cudaError_t launch_kernel(const CUtensorMap& tm_q, const CUtensorMap& tm_k, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<kMode, kQLoad>, tm_q, tm_k, tm_v, p);
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<kMode, kQLoad, kKLoad>, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace
@@ -871,6 +1009,22 @@ cudaError_t launch_sage_attn_pv16_qload(const CUtensorMap& tm_q_bf16, const CUte
                                         long long S_pad, cudaStream_t stream) {
   return launch_kernel<Mode::kSagePV16, true>(tm_q_bf16, tm_k16, tm_v_bf16, nullptr, k_scale, nullptr, 0.0f, o,
                                               o_sb, o_ss, o_sh, B, S, H, S_pad, stream, false, &qa);
+}
+
+cudaError_t launch_sage_attn_qkload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k_bf16,
+                                    const CUtensorMap& tm_v8, const QLoadArgs& qa, const float* v_scale, void* o,
+                                    long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                    long long S_pad, cudaStream_t stream) {
+  return launch_kernel<Mode::kSageFP8, true, true>(tm_q_bf16, tm_k_bf16, tm_v8, nullptr, nullptr, v_scale, 0.0f, o,
+                                                   o_sb, o_ss, o_sh, B, S, H, S_pad, stream, false, &qa);
+}
+
+cudaError_t launch_sage_attn_pv16_qkload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k_bf16,
+                                         const CUtensorMap& tm_v_bf16, const QLoadArgs& qa, void* o, long long o_sb,
+                                         long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
+                                         cudaStream_t stream) {
+  return launch_kernel<Mode::kSagePV16, true, true>(tm_q_bf16, tm_k_bf16, tm_v_bf16, nullptr, nullptr, nullptr, 0.0f,
+                                                    o, o_sb, o_ss, o_sh, B, S, H, S_pad, stream, false, &qa);
 }
 
 cudaError_t launch_attn_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,

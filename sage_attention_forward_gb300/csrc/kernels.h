@@ -107,6 +107,7 @@ struct PrepareArgs {
   void* k16 = nullptr;
   bool skip_v = false;       // V not prepared (the 16-bit P V mode reads the BF16 input)
   bool skip_q = false;       // Q not prepared (the forward quantises Q as it loads it)
+  bool skip_k = false;       // K not prepared either (the forward codes K as well; needs skip_q)
   void* q_mean16 = nullptr;  // Q smoothing: output, binary16 [B*H, S_pad/32, 128] block means in step units
                              // (nullptr: no Q smoothing); the FP16 codes (q16) are then f16(code + mean)
 };
@@ -140,6 +141,7 @@ cudaError_t launch_sage_attn_pv16(const CUtensorMap& tm_q16, const CUtensorMap& 
 // prepare would have written (optional RMSNorm + RoPE first, the same arithmetic).
 struct QLoadArgs {
   const void* q_norm_w = nullptr;   // BF16 [128], or nullptr: no RMSNorm
+  const void* k_norm_w = nullptr;   // the same for K (K coded on load)
   float rms_eps = 0.0f;
   const void* rope_cos = nullptr;   // BF16 [S, rope_dim], or nullptr: no RoPE
   const void* rope_sin = nullptr;
@@ -150,6 +152,16 @@ cudaError_t launch_sage_attn_qload(const CUtensorMap& tm_q_bf16, const CUtensorM
                                    const CUtensorMap& tm_v8, const QLoadArgs& qa, const float* k_scale,
                                    const float* v_scale, void* o, long long o_sb, long long o_ss, long long o_sh,
                                    int B, int S, int H, long long S_pad, cudaStream_t stream);
+// K coded on load as well: K through a BF16 [B, S, H, 128] tensor map, coded per tile by the
+// softmax warpgroups (the prepare's arithmetic); the block scales never leave shared memory.
+cudaError_t launch_sage_attn_qkload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k_bf16,
+                                    const CUtensorMap& tm_v8, const QLoadArgs& qa, const float* v_scale, void* o,
+                                    long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,
+                                    long long S_pad, cudaStream_t stream);
+cudaError_t launch_sage_attn_pv16_qkload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k_bf16,
+                                         const CUtensorMap& tm_v_bf16, const QLoadArgs& qa, void* o, long long o_sb,
+                                         long long o_ss, long long o_sh, int B, int S, int H, long long S_pad,
+                                         cudaStream_t stream);
 cudaError_t launch_sage_attn_pv16_qload(const CUtensorMap& tm_q_bf16, const CUtensorMap& tm_k16,
                                         const CUtensorMap& tm_v_bf16, const QLoadArgs& qa, const float* k_scale,
                                         void* o, long long o_sb, long long o_ss, long long o_sh, int B, int S, int H,

@@ -582,7 +582,7 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   p.vmax = a.vmax;
   p.kmean = a.k_mean;
   p.qmean16 = reinterpret_cast<__half*>(a.q_mean16);
-  p.task0 = a.skip_q ? 1 : 0;
+  p.task0 = a.skip_q ? (a.skip_k ? 2 : 1) : 0;
   // heads along grid.y (at most 65535 per launch, which the caller below guarantees)
   const int BH = a.B * a.H;
   if (a.k_mean != nullptr) {
@@ -594,14 +594,18 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // tasks [task0, 3 or 2) over grid.z
-  dim3 g1((nblk + 7) / 8, BH, (a.skip_v ? 2 : 3) - p.task0);
-  if (p.qmean16 != nullptr && p.task0 == 0)
-    prep_qk_vmax_kernel<true><<<g1, 256, 0, stream>>>(p);
-  else
-    prep_qk_vmax_kernel<false><<<g1, 256, 0, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // tasks [task0, 3 or 2) over grid.z (none left when the forward codes Q and K and V is
+  // not quantised)
+  const int tasks = (a.skip_v ? 2 : 3) - p.task0;
+  if (tasks > 0) {
+    dim3 g1((nblk + 7) / 8, BH, tasks);
+    if (p.qmean16 != nullptr && p.task0 == 0)
+      prep_qk_vmax_kernel<true><<<g1, 256, 0, stream>>>(p);
+    else
+      prep_qk_vmax_kernel<false><<<g1, 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (a.skip_v) return cudaSuccess;
 
   VParams vp;

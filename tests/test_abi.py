@@ -154,9 +154,18 @@ def test_sage_attention_one_call_rejects_bad_arguments():
     assert L.sage_attention_workspace_size(1, 2, 256, 0, 1, 0) < ws       # no V in the 16-bit mode
     assert L.sage_attention_workspace_size(1, 2, 256, 1, 0, 0) > ws       # K smoothing adds its sums
 
-    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256, qload=0, smooth_q=0):
+    # Q and K coded on load with the 16-bit P V: nothing is prepared, no workspace at all
+    assert L.sage_attention_workspace_size(1, 2, 256, 0, 1, 2) == 0
+    assert 0 < L.sage_attention_workspace_size(1, 2, 256, 0, 0, 2) < L.sage_attention_workspace_size(1, 2, 256, 0, 0, 1)
+
+    def call(smooth=0, pv=0, o=FAKE, ws_bytes=ws, S=256, qload=0, smooth_q=0, ws_ptr=FAKE):
         return L.sage_attention(FAKE, FAKE, FAKE, 1, S, 2, 128, st, st, st, 0.088, None, None, 1e-6, None, None, 0,
-                                smooth_q, smooth, pv, qload, o, st, FAKE, ws_bytes, None)
+                                smooth_q, smooth, pv, qload, o, st, ws_ptr, ws_bytes, None)
+
+    assert call(pv=0, qload=2, ws_ptr=None, ws_bytes=0) == 1     # e4m3 V still needs its workspace
+    if call(pv=1, qload=2, ws_ptr=None, ws_bytes=0) != 0:        # accepted; fails later only for want of a GPU
+        assert b"workspace" not in L.attn_last_error()
+    assert call(smooth=1, qload=2) == 3          # K's sequence mean needs a pass of its own
 
     assert call(smooth=2) == 1
     assert call(smooth_q=2) == 1

