@@ -169,7 +169,7 @@ class SmClock:
 
 def time_providers(calls, stream, clk, rounds=3, warm=2, reps=5):
     """Each provider alone: `warm` warm-up calls, then `reps` calls between two events
-    (and two SM clock samples), `rounds` rounds with the providers interleaved.
+    (and two SM clock samples); the providers take turns within each of `rounds` rounds.
     Returns name -> {"ms": median per-call ms, "sm_mhz": median clock, "mcycles": median
     per-call SM cycles / 1e6}."""
     import torch

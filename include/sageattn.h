@@ -10,20 +10,21 @@
  *                   attention, compilation and fusion", section "Attention:
  *                   from O(N^2) memory to blocks"; the RDNA2 DiT flash kernel
  *                   note, Contribution.)
- *   sage_prepare    the input stage of the SageAttention-style forward: Q/K to
- *                   INT8 with one FP32 scale per (batch, head, 32-row block),
- *                   Q's scale carrying softmax_scale * log2(e); V to FP8 e4m3
- *                   transposed to [B, H, 128, S_pad] with one FP32 scale per
- *                   channel; optionally QK RMSNorm and rotate-half RoPE first,
- *                   rounded like the eager PyTorch BF16 sequence.  (aiter pull
+ *   sage_prepare    the input stage of the SageAttention-style forward: INT8
+ *                   codes for Q and K, every 32 rows of a (batch, head) sharing
+ *                   one FP32 scale (Q's scales also hold softmax_scale * log2 e);
+ *                   e4m3 codes for V stored channel-major, [B, H, 128, S_pad],
+ *                   each channel with its own FP32 scale; optionally an RMSNorm and a
+ *                   rotate-half RoPE of Q and K beforehand, with the BF16
+ *                   rounding points of PyTorch's eager sequence.  (aiter pull
  *                   request "gfx1201_sage_prepare / gfx1201_sage_attention",
  *                   commit message of gfx1201_sage_prepare; Technical Details.)
- *   sage_attn_fwd   the attention kernel alone on prepared tensors: Q K^T on
+ *   sage_attn_fwd   the attention kernel by itself, on tensors a prepare wrote: Q K^T on
  *                   the INT8 codes, P V with P and V in FP8 e4m3, FP32
  *                   accumulation, online softmax, BF16 output.  (Same pull
- *                   request, commit message of gfx1201_sage_attention:
- *                   "gfx1201_sage_attention_fwd runs the kernel alone on
- *                   prepared tensors".)
+ *                   request, commit message of gfx1201_sage_attention, whose
+ *                   op also exposes the kernel on its own for inputs already
+ *                   prepared.)
  *   sage_attention  prepare + kernel as one call (that pull request's
  *                   gfx1201_sage_attention op), the prepared tensors kept in
  *                   the caller's workspace.

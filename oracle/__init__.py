@@ -11,13 +11,13 @@ Functions and the passages they follow:
                     ai-infra handbook chapter "Kernel acceleration: attention,
                     compilation and fusion" (section "Attention: from O(N^2)
                     memory to blocks").
-  norm_rope      -- QK RMSNorm then rotate-half RoPE "rounded like the eager
-                    PyTorch BF16 sequence" (aiter pull request
+  norm_rope      -- RMSNorm then rotate-half RoPE of a Q or K row, with the
+                    BF16 rounding points of PyTorch's eager ops (aiter pull request
                     "gfx1201_sage_prepare / gfx1201_sage_attention",
                     gfx1201_sage_prepare commit message).
-  quant_qk       -- Q/K to INT8, one FP32 scale per (batch, head, 32-row
-                    block), Q's scale carrying softmax_scale*log2(e) (same
-                    pull request, Technical Details).
+  quant_qk       -- INT8 codes for Q or K, each 32-row block of a (batch,
+                    head) with its own FP32 scale; Q's scales also hold
+                    softmax_scale*log2(e) (same pull request, Technical Details).
   k_mean         -- K smoothing: the per-(batch, head, channel) mean of K over
                     its tokens, subtracted before quantising K (ai-infra
                     handbook chapter above, section "SageAttention:
@@ -26,8 +26,9 @@ Functions and the passages they follow:
                     subtracted before quantising Q and kept, in units of the
                     block's step, as binary16 values that the score product
                     adds back (the correction term qbar . k).
-  quant_v        -- V to FP8 e4m3 transposed to [B, H, 128, S_pad], one FP32
-                    scale per channel (same pull request, Technical Details).
+  quant_v        -- e4m3 codes for V, stored channel-major [B, H, 128, S_pad],
+                    each channel with its own FP32 scale (same pull request,
+                    Technical Details).
   prepare        -- the three above in order, as the prepare stage runs them.
   sage_attention -- FP64 attention evaluated on prepared tensors: the exact
                     value of the INT8/e4m3 format the Sage forward consumes

@@ -222,8 +222,8 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 /* ------------------------------------------------- Sage prepare: RMSNorm */
 
 /*
- * RMSNorm of one 128-channel head row, "rounded like the eager PyTorch BF16
- * sequence" (aiter pull request, gfx1201_sage_prepare commit message):
+ * RMSNorm of one 128-channel head row, with the BF16 rounding points of
+ * PyTorch's eager ops (aiter pull request, gfx1201_sage_prepare commit message):
  *   y   = bf16( x * r ),   r = 1 / sqrt( mean(x^2) + eps )
  *   out = bf16( y * w )
  * with x widened from BF16 and every operation an IEEE binary32 operation.
@@ -264,8 +264,8 @@ static void rmsnorm_row(const uint16_t* x, const uint16_t* w, float eps, uint16_
 
 /*
  * Rotate-half RoPE on the first rope_dim channels of one head row at sequence
- * position s (aiter pull request, gfx1201_sage_prepare commit message:
- * "rotate-half RoPE (rope_dim 32/64/96/128)").  With h = rope_dim / 2:
+ * position s, for rope_dim of 32, 64, 96 or 128 (aiter pull request,
+ * gfx1201_sage_prepare commit message).  With h = rope_dim / 2:
  *   rot[c] = -x[c + h] for c < h,   rot[c] = x[c - h] for h <= c < rope_dim
  *   out[c] = bf16( bf16(x[c] * cos[s, c]) + bf16(rot[c] * sin[s, c]) )
  * which is the eager BF16 sequence x*cos + rotate_half(x)*sin (each product
@@ -310,8 +310,9 @@ void oracle_norm_rope(const uint16_t* x, int B, int S, int H, const uint16_t* w,
 /* ---------------------------------------------- Sage prepare: Q/K to INT8 */
 
 /*
- * "Q/K -> INT8 with one FP32 scale per (batch, head, 32-row block), Q carrying
- * softmax_scale * log2(e)" (aiter pull request, Technical Details).
+ * INT8 codes for Q and K: each 32-row block of a (batch, head) has one FP32
+ * scale, and Q's scales also hold softmax_scale * log2(e) (aiter pull request,
+ * Technical Details).
  *
  * Readings: symmetric quantisation with the block's absolute maximum a over
  * its valid rows (rows < S):
@@ -512,8 +513,8 @@ void oracle_quant_q_smooth(const uint16_t* x, int B, int S, int H, int64_t S_pad
 /* ----------------------------------------------- Sage prepare: V to e4m3 */
 
 /*
- * "V -> FP8 e4m3, transposed to [B, H, 128, S_pad], one FP32 scale per
- * channel" (aiter pull request, Technical Details).
+ * e4m3 codes for V, stored channel-major as [B, H, 128, S_pad], each channel
+ * with one FP32 scale (aiter pull request, Technical Details).
  *
  * Readings: one scale per (batch, head, channel) from the channel's absolute
  * maximum a over all valid positions s < S; inv = 448 / a (448 being the
@@ -551,8 +552,8 @@ void oracle_quant_v(const uint16_t* x, int B, int S, int H, int64_t S_pad, uint8
  * FP64 attention on prepared tensors, the function the Sage forward
  * approximates (aiter pull request "gfx1201_sage_prepare /
  * gfx1201_sage_attention", commit message of gfx1201_sage_attention: scores
- * from the INT8 codes, Q's scale carrying softmax_scale * log2(e), V from its
- * e4m3 codes and per-channel scales):
+ * from the INT8 codes, with softmax_scale * log2(e) inside Q's scales, V from
+ * its e4m3 codes and per-channel scales):
  *   t_j = (sum_d q_i8[r, d] k_i8[j, d]) * q_scale[r / 32] * k_scale[j / 32]   (log2 units)
  *   O[r, d] = sum_{j < S} 2^(t_j - max t) v[j, d] / sum_{j < S} 2^(t_j - max t),
  *   v[j, d] = e4m3(v_fp8[d, j]) * v_scale[d]

@@ -3,9 +3,9 @@
 // quantise-on-load of Q (one thread per row), so that both produce the same
 // codes bit for bit.  Follows the aiter pull request "gfx1201_sage_prepare /
 // gfx1201_sage_attention" (commit message of gfx1201_sage_prepare; Technical
-// Details): INT8 codes with one scale per 32-row block, Q's scale carrying
-// softmax_scale * log2 e, after an optional QK RMSNorm and rotate-half RoPE
-// rounded like eager BF16.
+// Details): INT8 codes with one scale per 32-row block, softmax_scale * log2 e
+// folded into Q's scales, after an optional RMSNorm and rotate-half RoPE of Q
+// and K with PyTorch's eager BF16 rounding points.
 //
 // Instruction selection keeps the instruction count low while every result
 // stays that of the rounded operation it implements: BF16 roundings of binary32

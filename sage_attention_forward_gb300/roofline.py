@@ -5,8 +5,8 @@ fractions are computed from; they do not depend on how a kernel is written.
 
 * Attention FLOPs: 4 * B * H * S^2 * D -- two GEMMs of 2*S*S*D each per
   (batch, head).  This is the count the aiter pull request
-  "gfx1201_sage_prepare / gfx1201_sage_attention" uses for TFLOPS (How to
-  reproduce: "TFLOPS = 4 * B * H * S^2 * 128 / time") and the `4 * n * n * d`
+  "gfx1201_sage_prepare / gfx1201_sage_attention" divides by the time to
+  report TFLOPS (How to reproduce, with D = 128) and the `4 * n * n * d`
   of the ai-infra handbook chapter "Kernel acceleration: attention,
   compilation and fusion" (block_profile table, row "attention (Flash)").
 * Attention minimum bytes (flash form): read Q, K, V once and write O once,

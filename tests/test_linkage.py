@@ -1,6 +1,6 @@
 """The library's own linkage, the check the RDNA2 DiT flash-kernel note reports
-(Results and Reproducibility / Provenance: dynamic linkage to the base runtime and
-system libraries only, no vendor BLAS or attention library): the built
+(Results and Reproducibility / Provenance: the note's kernel links against the base
+runtime and the operating system's libraries and nothing more): the built
 libsageattn.so needs the CUDA runtime and the C/C++ system libraries and nothing
 else -- no cuBLAS, cuDNN or other kernel library.  The TMA descriptor
 encoder is reached through the runtime's driver entry point, so libcuda is not

@@ -6,6 +6,7 @@ ai-infra handbook's blocked online-softmax example ("Kernel acceleration:
 attention, compilation and fusion", section "Attention: from O(N^2) memory to
 blocks"), and torch's own scaled_dot_product_attention in float64.
 """
+import functools
 import math
 import os
 
@@ -29,28 +30,29 @@ def sdpa64(q, k, v, scale):
     return F.scaled_dot_product_attention(qd, kd, vd, scale=scale).permute(0, 2, 1, 3).numpy()
 
 
-def blocked_online_softmax(q, k, v, scale, block):
-    """The handbook's blocked form in FP64: per Q block, stream K/V blocks,
-    keep a running max m, running sum l and an unnormalised accumulator,
-    rescale both by exp(m_old - m_new), divide by l at the end."""
-    qd, kd, vd = (t.double().permute(0, 2, 1, 3).numpy() for t in (q, k, v))
-    B, H, N, D = qd.shape
-    out = np.zeros_like(qd)
-    for i in range(0, N, block):
-        qi = qd[:, :, i:i + block]
-        m = np.full(qi.shape[:3] + (1,), -np.inf)
-        l = np.zeros(qi.shape[:3] + (1,))
-        acc = np.zeros(qi.shape)
-        for j in range(0, N, block):
-            s = (qi @ kd[:, :, j:j + block].transpose(0, 1, 3, 2)) * scale
-            m_new = np.maximum(m, s.max(-1, keepdims=True))
-            p = np.exp(s - m_new)
-            corr = np.exp(m - m_new)
-            l = l * corr + p.sum(-1, keepdims=True)
-            acc = acc * corr + p @ vd[:, :, j:j + block]
-            m = m_new
-        out[:, :, i:i + block] = acc / l
-    return out.transpose(0, 2, 1, 3)
+def chunked_softmax_attention(q, k, v, scale, chunk):
+    """FP64 attention the blocked way, so that the full S x S score matrix never
+    exists: the keys are taken `chunk` at a time, each chunk is reduced to a
+    partial softmax state (per query row: the chunk's largest score, the sum of
+    exp(t - that maximum) and the same weights applied to the chunk's V rows), and
+    the states are merged left to right by bringing both to the larger maximum.
+    This is the running-maximum bookkeeping of the handbook's blocked online
+    softmax written as a fold; only the final division by the weight sum remains."""
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))   # [B, S, H, D]
+
+    def reduce_chunk(c0):
+        t = np.einsum("bqhd,bkhd->bhqk", qd, kd[:, c0:c0 + chunk]) * scale
+        top = t.max(axis=-1)
+        w = np.exp(t - top[..., None])
+        return top, w.sum(axis=-1), np.einsum("bhqk,bkhd->bhqd", w, vd[:, c0:c0 + chunk])
+
+    def merge(a, b):
+        peak = np.maximum(a[0], b[0])
+        fa, fb = np.exp(a[0] - peak), np.exp(b[0] - peak)
+        return peak, a[1] * fa + b[1] * fb, a[2] * fa[..., None] + b[2] * fb[..., None]
+
+    _, weight, weighted_v = functools.reduce(merge, map(reduce_chunk, range(0, qd.shape[1], chunk)))
+    return (weighted_v / weight[..., None]).transpose(0, 2, 1, 3)
 
 
 def test_single_key_returns_its_value_exactly():
@@ -141,7 +143,7 @@ def test_blocked_online_softmax_equals_definition_at_handbook_example():
     q, k, v = (torch.randn(B, N, H, D, generator=g).to(torch.bfloat16) for _ in range(3))
     scale = 1 / math.sqrt(D)
     o = oracle.attention(q, k, v, scale)
-    ob = blocked_online_softmax(q, k, v, scale, block)
+    ob = chunked_softmax_attention(q, k, v, scale, block)
     # the handbook prints agreement at atol 1e-5 in float32; in FP64 the two forms agree to rounding
     assert np.allclose(o, ob, atol=gd["atol"])
     np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)

@@ -1,8 +1,8 @@
 """Pins for the oracle's Q smoothing (CPU only).
 
 The ai-infra handbook ("Kernel acceleration: attention, compilation and
-fusion", section "SageAttention: quantizing attention too") has SageAttention
-subtract the block means of Q as well as of K before the INT8 quantisation.
+fusion", section "SageAttention: quantizing attention too") describes
+SageAttention removing a block mean from Q, and from K, ahead of INT8.
 Unlike K's, Q's mean does not cancel in the softmax: q . k = (q - qbar) . k +
 qbar . k, so the mean is kept with each 32-row block, in units of the block's
 step as binary16 values, and the score product takes Q's operand as
