@@ -35,7 +35,8 @@
  * sage_attn_fwd_pv16 (P V in 16 bits with V unquantised), all from the
  * handbook's SageAttention section; sage_prepare_noalloc (no
  * workspace argument); attn_selftest_wait_timeout (exercises the failure path);
- * attn_sm_clock_sample (SM clock counters, for timing);
+ * attn_sm_clock_sample (SM clock counters, for timing); sage_e4m3_encode (the
+ * e4m3 conversion the prepare and the FP8 P V use, on its own);
  * sizes and status helpers.
  *
  * Conventions shared by every call
@@ -439,6 +440,21 @@ ATTN_API attn_status attn_selftest_wait_timeout(const void* q, const void* k, co
  * ATTN_ERR_ALIGNMENT; launch failure -> ATTN_ERR_CUDA.
  */
 ATTN_API attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_stream_t stream);
+
+/*
+ * sage_e4m3_encode -- FP8 e4m3 codes of n binary32 values: round to nearest,
+ * ties to the even code, magnitudes beyond 448 saturate to +-448, NaN gives
+ * 0x7f (the V format of the aiter pull request "gfx1201_sage_prepare /
+ * gfx1201_sage_attention", Technical Details, with the rounding sage_prepare
+ * documents).  It runs the same packing as sage_prepare's V codes and the FP8
+ * P of the Sage forward, so the conversion they share can be checked on its
+ * own, and serves callers that quantise other tensors the same way.
+ *   x : device float32 [n];  y : device uint8 [n], written (any alignment)
+ *   n : number of values; 0 returns ATTN_OK at once
+ * Enqueues one kernel on `stream`.  Errors: n < 0, NULL x or y (n > 0) ->
+ * ATTN_ERR_INVALID_ARG; launch failure -> ATTN_ERR_CUDA.
+ */
+ATTN_API attn_status sage_e4m3_encode(const float* x, uint8_t* y, int64_t n, attn_stream_t stream);
 
 /* attn_last_error -- message of the calling thread's last failed call ("" if none). */
 ATTN_API const char* attn_last_error(void);

@@ -85,7 +85,6 @@ def lib():
                                                 ctypes.c_int, ctypes.c_int64, c_p, ctypes.c_int64, ctypes.c_int, c_p,
                                                 ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
-        L.oracle_init()
         _lib = L
     return _lib
 

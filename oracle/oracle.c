@@ -78,13 +78,11 @@ double oracle_e4m3_decode(uint8_t c) {
 }
 
 /* The 127 finite non-negative e4m3 magnitudes, indexed by code (they increase
- * with the code), filled once from the definition above. */
+ * with the code), filled from the definition above when the library is loaded,
+ * before any thread can encode. */
 static double e4m3_mag[127];
-static int e4m3_ready = 0;
-static void e4m3_init(void) {
-    if (e4m3_ready) return;
+__attribute__((constructor)) static void e4m3_init(void) {
     for (int c = 0; c < 127; c++) e4m3_mag[c] = oracle_e4m3_decode((uint8_t)c);
-    e4m3_ready = 1;
 }
 
 /* Encode a finite binary32 as e4m3: round to nearest, ties to the even code,
@@ -95,7 +93,6 @@ uint8_t oracle_e4m3_encode(float x) {
     uint8_t sign = signbit(x) ? 0x80 : 0x00;
     double a = fabs((double)x);
     if (isnan(x)) return 0x7f;
-    e4m3_init();
     if (a >= 448.0) return sign | 126;
     int lo = 0, hi = 126;              /* invariant: mag[lo] <= a < mag[hi] */
     while (hi - lo > 1) {
@@ -149,6 +146,9 @@ void oracle_f16_encode_array(const double* x, uint16_t* out, int64_t n) {
 }
 
 void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
+    /* element by element; the threads only share the work (exhaustive checks encode
+     * every binary32 of a range) */
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; i++) out[i] = oracle_e4m3_encode(x[i]);
 }
 void oracle_e4m3_decode_array(const uint8_t* c, double* out, int64_t n) {
@@ -589,7 +589,6 @@ void oracle_sage_attention(const int8_t* q8, const int8_t* k8, const uint8_t* v8
     (void)B;
     const int nt = oracle_team_size(nthreads);
     (void)nt;
-    e4m3_init();
 #pragma omp parallel num_threads(nt)
     {
         double* t = (double*)malloc(sizeof(double) * (size_t)S);
@@ -687,8 +686,6 @@ void oracle_sage_attention_v16(const int8_t* q8, const int8_t* k8, const float* 
         free(t);
     }
 }
-
-void oracle_init(void) { e4m3_init(); }
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -24,7 +24,7 @@ import torch
 from .build import LIB as _LIB_PATH
 
 __all__ = ["AttnError", "attn_fwd_bf16", "sage_prepare", "sage_prepare_noalloc", "sage_attn_fwd", "sage_attention",
-           "Prepared",
+           "Prepared", "e4m3_encode",
            "sage_padded_len", "attn_get_device_status", "lib", "STATUS"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_ALIGNMENT", 3: "ATTN_ERR_UNSUPPORTED",
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.attn_selftest_wait_timeout.restype = i
         L.attn_sm_clock_sample.argtypes = [_vp, i, _vp]
         L.attn_sm_clock_sample.restype = i
+        L.sage_e4m3_encode.argtypes = [_vp, _vp, ctypes.c_int64, _vp]
+        L.sage_e4m3_encode.restype = i
         L.attn_get_device_status.argtypes = [_vp]
         L.attn_get_device_status.restype = i
         L.attn_last_error.argtypes = []
@@ -401,6 +403,20 @@ def attn_selftest_wait_timeout(device=None, stream=None) -> str:
     bufs = [torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev) for _ in range(4)]
     code = lib().attn_selftest_wait_timeout(*(b.data_ptr() for b in bufs), _stream_ptr(stream))
     return STATUS.get(code, str(code))
+
+
+def e4m3_encode(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """e4m3 codes (uint8, x's shape) of a float32 CUDA tensor: nearest even, saturating
+    at +-448, through the conversion the prepare's V pass and the FP8 P V use."""
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    elif out.dtype != torch.uint8 or out.shape != x.shape or not out.is_contiguous() or out.device != x.device:
+        raise ValueError("out must be a contiguous uint8 tensor of x's shape on x's device")
+    _check(lib().sage_e4m3_encode(x.data_ptr(), out.data_ptr(), x.numel(), _stream_ptr(stream)))
+    return out
 
 
 def sm_clock_sample(out: torch.Tensor, stream=None) -> torch.Tensor:

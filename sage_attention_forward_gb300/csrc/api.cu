@@ -755,6 +755,16 @@ attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_stream_t strea
   return ATTN_OK;
 }
 
+attn_status sage_e4m3_encode(const float* x, uint8_t* y, int64_t n, attn_stream_t stream) {
+  if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "sage_e4m3_encode: n=%lld must be >= 0", (long long)n);
+  if (n == 0) return ATTN_OK;
+  if (x == nullptr || y == nullptr) return fail(ATTN_ERR_INVALID_ARG, "sage_e4m3_encode: x or y is NULL");
+  TRY(check_device());
+  cudaError_t e = sa::launch_e4m3_encode(x, y, (long long)n, sa::device_sm_count(), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "sage_e4m3_encode launch");
+  return ATTN_OK;
+}
+
 const char* attn_last_error(void) { return g_msg; }
 
 const char* attn_status_name(attn_status s) {

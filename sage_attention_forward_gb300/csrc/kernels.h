@@ -115,6 +115,8 @@ cudaError_t launch_sage_prepare(const PrepareArgs& a, cudaStream_t stream);
 // Q's score operand with Q smoothing, f16(code + mean), from the INT8 codes and the block means.
 cudaError_t launch_widen_q_mean(const int8_t* q8, const void* qmean16, void* q16, long long n_codes, int num_sms,
                                cudaStream_t stream);
+// e4m3 codes of n binary32 values through the prepare's and the attention's packing.
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* y, long long n, int num_sms, cudaStream_t stream);
 
 // Device address, in the current context, of the static scratch used by the
 // allocation-free prepare entry point; it holds kNoAllocMaxHeads * 128 words.

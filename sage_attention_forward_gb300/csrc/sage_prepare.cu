@@ -530,6 +530,24 @@ __global__ void __launch_bounds__(128) prep_v_kernel(const VParams p) {
 // the process exits, and every call of that entry point on a device shares it.
 __device__ __align__(256) static uint32_t g_prepare_scratch[kNoAllocMaxHeads * 128];
 
+// e4m3 codes of n binary32 values (nearest even, saturating to +-448): four per
+// thread through pack_e4m3x4, the packing of prep_v_kernel's V codes and of the
+// attention kernel's FP8 P, so that the hardware conversion both rely on can be
+// checked value by value.  Grid-stride; every access is guarded by n.
+__global__ void __launch_bounds__(256) e4m3_encode_kernel(const float* __restrict__ x, uint8_t* __restrict__ y,
+                                                          long long n) {
+  const long long stride = 4LL * gridDim.x * blockDim.x;
+  for (long long i = 4LL * ((long long)blockIdx.x * blockDim.x + threadIdx.x); i < n; i += stride) {
+    float f[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = i + e < n ? x[i + e] : 0.0f;
+    const uint32_t w = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (i + e < n) y[i + e] = (uint8_t)(w >> (8 * e));
+  }
+}
+
 }  // namespace
 
 cudaError_t noalloc_prepare_scratch(uint32_t** out) {
@@ -678,6 +696,15 @@ cudaError_t launch_widen_q_mean(const int8_t* q8, const void* qmean16, void* q16
   if (blocks < 1) blocks = 1;
   widen_q_mean_kernel<<<(unsigned)blocks, 256, 0, stream>>>(q8, reinterpret_cast<const __half*>(qmean16),
                                                              reinterpret_cast<__half*>(q16), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* y, long long n, int num_sms, cudaStream_t stream) {
+  long long blocks = (n + 4LL * 256 - 1) / (4LL * 256);
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  e4m3_encode_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, y, n);
   return cudaGetLastError();
 }
 

@@ -200,6 +200,14 @@ def test_smoothed_prepare_and_forward_reject_bad_arguments():
                                          ws, None) == 1
 
 
+def test_e4m3_encode_rejects_bad_arguments():
+    L = sa.lib()
+    assert L.sage_e4m3_encode(None, None, 0, None) == 0          # nothing to encode: nothing is touched
+    assert L.sage_e4m3_encode(FAKE, FAKE, -1, None) == 1
+    assert L.sage_e4m3_encode(None, FAKE, 16, None) == 1
+    assert L.sage_e4m3_encode(FAKE, None, 16, None) == 1
+
+
 def test_product_path_does_not_import_the_oracle():
     import subprocess
     import sys

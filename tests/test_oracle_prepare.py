@@ -67,6 +67,23 @@ def test_e4m3_encode_matches_torch_in_range():
     assert np.array_equal(mine, ref)
 
 
+def test_e4m3_encode_matches_torch_on_every_binary32_below_448():
+    """Every binary32 bit pattern of magnitude below 448, with both signs (2.27e9
+    values, denormals and signed zeros included): the oracle's encoder against
+    torch's float8_e4m3fn cast, nearest-even in that range (above it torch's cast
+    does not saturate, so saturation is pinned separately)."""
+    top = 0x43E00000                        # the bit pattern of 448.0
+    chunk = 1 << 26
+    for sign in (0, 0x80000000):
+        for start in range(0, top, chunk):
+            bits = np.arange(start, min(start + chunk, top), dtype=np.uint32) | np.uint32(sign)
+            x = bits.view(np.float32)
+            mine = oracle.e4m3_encode(x)
+            ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            bad = np.flatnonzero(mine != ref)
+            assert bad.size == 0, f"{bad.size} mismatches, the first at bits {int(bits[bad[0]]):#010x}"
+
+
 def test_e4m3_midpoints_round_to_even_code():
     mags = oracle.e4m3_decode(np.arange(126, dtype=np.uint8))
     nxt = oracle.e4m3_decode(np.arange(1, 127, dtype=np.uint8))
