@@ -77,21 +77,23 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* src, uint32_t (&w)[8
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-// Rows 32*blk + 4*step + g (step = 0..7) of tensor `task` (0: Q, 1: K), channels
+// Rows row0 + 4*step + g (step < kSteps) of tensor `task` (0: Q, 1: K), channels
 // [16L, 16L + 16), after the optional RMSNorm and RoPE, as packed BF16 pairs;
-// rows >= S are zero.  Shared by the quantiser and the K-mean partial sums, so
-// both see the same bits.
-__device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, int blk, int lane,
-                                          uint32_t (&x)[8][8]) {
+// rows >= S are zero.  A warp covers 4 * kSteps rows: a whole 32-row block
+// (kSteps = 8) or half of one (4).  Shared by the quantiser and the K-mean
+// partial sums, so both see the same bits.
+template <int kSteps>
+__device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, int row0, int lane,
+                                          uint32_t (&x)[kSteps][8]) {
   const int b = bh / p.H, h = bh % p.H;
   const int g = lane >> 3;
   const int L = lane & 7;
   const __nv_bfloat16* base = p.x[task] + (long long)b * p.sb[task] + (long long)h * p.sh[task] + 16 * L;
   const long long ss = p.ss[task];
-  // ---------------------------------------------------------- load 8 rows x 16 channels
+  // ---------------------------------------------------------- load kSteps rows x 16 channels
 #pragma unroll
-  for (int step = 0; step < 8; ++step) {
-    const int s = 32 * blk + 4 * step + g;
+  for (int step = 0; step < kSteps; ++step) {
+    const int s = row0 + 4 * step + g;
     if (s < p.S) {
       load16(base + (long long)s * ss, x[step]);
     } else {
@@ -111,7 +113,7 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
     // once, and the group's lanes fetch each step's factor from lane L = step by a shuffle
     float mine = 0.0f;
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
+    for (int step = 0; step < kSteps; ++step) {
       float acc = sumsq16(x[step]);
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
       acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
@@ -120,7 +122,7 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
     }
     const float r_mine = rms_factor(mine, p.eps);
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
+    for (int step = 0; step < kSteps; ++step) {
       const float r = __shfl_sync(0xffffffffu, r_mine, (lane & ~7) | step);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -128,10 +130,10 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
     }
     // rows >= S stay exact zeros (with rms_eps = 0 their factor is infinite); only the last
     // block has such rows
-    if (32 * blk + 32 > p.S) {
+    if (row0 + 4 * kSteps > p.S) {
 #pragma unroll
-      for (int step = 0; step < 8; ++step)
-        if (32 * blk + 4 * step + g >= p.S)
+      for (int step = 0; step < kSteps; ++step)
+        if (row0 + 4 * step + g >= p.S)
 #pragma unroll
           for (int i = 0; i < 8; ++i) x[step][i] = 0u;
     }
@@ -147,11 +149,11 @@ __device__ __forceinline__ void load_rows(const QKParams& p, int task, int bh, i
     const int src_lane = (lane & ~7) | src;
     const uint32_t neg = lo_half ? 0x80008000u : 0u;
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
+    for (int step = 0; step < kSteps; ++step) {
       uint32_t partner[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) partner[i] = __shfl_sync(0xffffffffu, x[step][i], src_lane);
-      const int s = 32 * blk + 4 * step + g;
+      const int s = row0 + 4 * step + g;
       if (in_rope && s < p.S) {
         uint32_t cw[8], sw[8];
         load16(p.rope_cos + (long long)s * p.rope_dim + 16 * L, cw);
@@ -195,15 +197,43 @@ __device__ __forceinline__ void block_sums16(const uint32_t (&x)[8][8], float (&
   }
 }
 
-// kQSmooth: the instance that smooths Q (its block mean, binary16 mean output), with room
-// for the extra registers; the plain instance keeps two CTAs per SM
+// Barrier 1 + group for the kWarps warps of one group (immediate ids, so that a kernel
+// reserves only the barriers it names rather than all sixteen).
+template <int kWarps>
+__device__ __forceinline__ void group_bar_sync(int group) {
+  switch (group) {
+    case 0: asm volatile("bar.sync 1, %0;" ::"n"(32 * kWarps) : "memory"); break;
+    case 1: asm volatile("bar.sync 2, %0;" ::"n"(32 * kWarps) : "memory"); break;
+    case 2: asm volatile("bar.sync 3, %0;" ::"n"(32 * kWarps) : "memory"); break;
+    default: asm volatile("bar.sync 4, %0;" ::"n"(32 * kWarps) : "memory"); break;
+  }
+}
+
+// Blocks of 32 rows per CTA of the quantiser: the Q-smoothing instance gives each block
+// one warp (its block sums run over all 32 rows of a lane group in a fixed order); the
+// other gives each block two warps of 16 rows, which halves the rows a thread holds, so
+// that four CTAs fit an SM instead of two: the kernel waits on HBM, and more resident
+// warps keep more loads in flight (measured on a GB300: the prepare at Wan-720p 0.80 ->
+// 0.71 ms, at FLUX-2048 with RMSNorm + RoPE 0.30 -> 0.26 ms; four warps of 8 rows at five
+// CTAs per SM was slower at Wan-720p).
+constexpr int kQuantWarpsPerBlock = 2;   // the instance without Q smoothing (1, 2 or 4)
+__host__ __device__ constexpr int quant_blocks_per_cta(bool q_smooth) {
+  return q_smooth ? 8 : 8 / kQuantWarpsPerBlock;
+}
+
+// kQSmooth: the instance that smooths Q (its block mean, binary16 mean output)
 template <bool kQSmooth>
-__global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(const QKParams p) {
+__global__ void __launch_bounds__(256, kQSmooth ? 1 : 4) prep_qk_vmax_kernel(const QKParams p) {
   griddep_launch_dependents();   // the next kernel may set up meanwhile (it waits for this grid)
+  constexpr int kBlocksPerCta = quant_blocks_per_cta(kQSmooth);
+  constexpr int kWarpsPerBlock = 8 / kBlocksPerCta;   // 1, 2 or 4
+  constexpr int kSteps = 8 / kWarpsPerBlock;          // rows per lane: 8, 4 or 2
   const int task = blockIdx.z + p.task0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int bh, blk;
-  block_coords(warp, bh, blk);
+  const int bh = (int)blockIdx.y;
+  const int blk = (int)blockIdx.x * kBlocksPerCta + warp / kWarpsPerBlock;
+  const int half = warp % kWarpsPerBlock;             // which part of the block this warp holds
+  const int row0 = 32 * blk + 4 * kSteps * half;      // this warp's first row
   const int b = bh / p.H, h = bh % p.H;
   const int g = lane >> 3;   // row inside a 4-row step
   const int L = lane & 7;    // channel group [16L, 16L+16)
@@ -218,8 +248,8 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
     for (int i = 0; i < 8; ++i) m2[i] = 0u;
     if (blk < p.nblk) {
 #pragma unroll
-      for (int step = 0; step < 8; ++step) {
-        const int s = 32 * blk + 4 * step + g;
+      for (int step = 0; step < kSteps; ++step) {
+        const int s = row0 + 4 * step + g;
         if (s < p.S) {
           uint32_t w[8];
           load16(base + (long long)s * ss, w);
@@ -249,9 +279,9 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
     return;
   }
 
-  if (blk >= p.nblk) return;
-  uint32_t x[8][8];
-  load_rows(p, task, bh, blk, lane, x);
+  if (blk >= p.nblk) return;   // (both warps of a block together)
+  uint32_t x[kSteps][8];
+  load_rows<kSteps>(p, task, bh, row0, lane, x);
 
   // ---------------------------------------------------------- K or Q smoothing (optional)
   // the value quantised is fl32(x - mean[channel]); it is formed again, bit for bit, for
@@ -260,13 +290,18 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
   float mu[16];
   const bool qsmooth = kQSmooth && task == 0;
   const bool smooth = (task == 1 && p.kmean != nullptr) || qsmooth;
-  if (qsmooth) {
-    block_sums16(x, mu);
-    // valid rows; a block wholly past S has a zero sum and gets the mean +0
-    const float n = (float)max(1, min(32, p.S - 32 * blk));
+  bool have_mu = false;
+  if constexpr (kQSmooth) {
+    if (qsmooth) {
+      block_sums16(x, mu);
+      // valid rows; a block wholly past S has a zero sum and gets the mean +0
+      const float n = (float)max(1, min(32, p.S - 32 * blk));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mu[i] = __fdiv_rn(mu[i], n);
-  } else {
+      for (int i = 0; i < 16; ++i) mu[i] = __fdiv_rn(mu[i], n);
+      have_mu = true;
+    }
+  }
+  if (!have_mu) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) mu[i] = smooth ? __ldg(p.kmean + (long long)bh * 128 + 16 * L + i) : 0.0f;
   }
@@ -275,8 +310,8 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
   float a = 0.0f;
   if (smooth) {
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
-      const int s = 32 * blk + 4 * step + g;
+    for (int step = 0; step < kSteps; ++step) {
+      const int s = row0 + 4 * step + g;
       if (s < p.S) {
         float f[16];
         unpack16(x[step], f);
@@ -288,13 +323,23 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
     // |x| of BF16 values is exact, so the maximum is taken on the BF16 pairs (rows >= S are 0)
     uint32_t m2 = 0u;
 #pragma unroll
-    for (int step = 0; step < 8; ++step)
+    for (int step = 0; step < kSteps; ++step)
 #pragma unroll
       for (int i = 0; i < 8; ++i) m2 = bf2_max(m2, bf2_abs(x[step][i]));
     a = fmaxf(bf_lo(m2), bf_hi(m2));
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));
+  if constexpr (kWarpsPerBlock > 1) {
+    // the block's maximum over its warps' parts: each posts its own, then a barrier of the
+    // block's warps (named barrier 1 + block in the CTA; barrier 0 is left to __syncthreads)
+    __shared__ float part_max[8];
+    if (lane == 0) part_max[warp] = a;
+    group_bar_sync<kWarpsPerBlock>(warp / kWarpsPerBlock);
+    const int w0 = warp - half;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarpsPerBlock; ++w2) a = fmaxf(a, part_max[w0 + w2]);
+  }
   float inv;
   uint32_t m16[8];   // Q smoothing: the block mean in step units, binary16 pairs
   if (qsmooth) {
@@ -333,8 +378,8 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
   auto emit_codes = [&](auto kClamp, auto kSmooth) {
     constexpr bool kC = decltype(kClamp)::value;
 #pragma unroll
-    for (int step = 0; step < 8; ++step) {
-      const int s = 32 * blk + 4 * step + g;
+    for (int step = 0; step < kSteps; ++step) {
+      const int s = row0 + 4 * step + g;
       const bool live = s < p.S;
       auto code = [&](float f, int i) {
         if constexpr (decltype(kSmooth)::value) {
@@ -377,7 +422,7 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 2) prep_qk_vmax_kernel(con
     if (isinf(inv)) emit_codes(std::true_type{}, std::false_type{});
     else emit_codes(std::false_type{}, std::false_type{});
   }
-  if (lane == 0) p.scales[task][(long long)bh * p.nblk + blk] = block_scale(a, p.c_log2, task == 0);
+  if (lane == 0 && half == 0) p.scales[task][(long long)bh * p.nblk + blk] = block_scale(a, p.c_log2, task == 0);
 }
 
 // Q smoothing on the two-call path: Q's score operand f16(code + mean[block]) from the
@@ -432,7 +477,7 @@ __global__ void __launch_bounds__(256) prep_kmean_partial_kernel(const QKParams 
   const int g = lane >> 3;
   const int L = lane & 7;
   uint32_t x[8][8];
-  load_rows(p, 1, bh, blk, lane, x);
+  load_rows<8>(p, 1, bh, 32 * blk, lane, x);
   float acc[16];
   block_sums16(x, acc);
   if (g == 0) {
@@ -616,8 +661,10 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   // not quantised)
   const int tasks = (a.skip_v ? 2 : 3) - p.task0;
   if (tasks > 0) {
-    dim3 g1((nblk + 7) / 8, BH, tasks);
-    if (p.qmean16 != nullptr && p.task0 == 0)
+    const bool q_smooth = p.qmean16 != nullptr && p.task0 == 0;
+    const int per_cta = quant_blocks_per_cta(q_smooth);
+    dim3 g1((nblk + per_cta - 1) / per_cta, BH, tasks);
+    if (q_smooth)
       prep_qk_vmax_kernel<true><<<g1, 256, 0, stream>>>(p);
     else
       prep_qk_vmax_kernel<false><<<g1, 256, 0, stream>>>(p);
