@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(256, kQSmooth ? 1 : 4) prep_qk_vmax_kernel(con
     return;
   }
 
-  if (blk >= p.nblk) return;   // (both warps of a block together)
+  if (blk >= p.nblk) return;   // (all warps of a block leave together)
   uint32_t x[kSteps][8];
   load_rows<kSteps>(p, task, bh, row0, lane, x);
 
