@@ -511,7 +511,8 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
     Q, K, V in (H2D), runs both attention paths and copies both outputs out (D2H), all
     inside the timed region.  As a user streaming many steps would, consecutive steps
     overlap on three streams with double-buffered device tensors: step i+1's inputs
-    arrive while step i computes, step i-1's outputs leave meanwhile."""
+    arrive while step i computes, step i-1's outputs leave meanwhile, and a step's BF16
+    output leaves while its Sage call runs."""
     B, S, H, D = inp.q.shape
     hq = inp.q.contiguous().cpu().pin_memory()
     hk = inp.k.contiguous().cpu().pin_memory()
@@ -525,7 +526,7 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    in_done, bf16_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
     def run(n):
         for i in range(n):
@@ -543,11 +544,15 @@ def run_e2e(args, sa, torch, dev, inp, scale, S_pad, kw, F, world, dist):
             if i >= 2:
                 comp.wait_event(out_done[bf])         # step i-2's outputs have left these buffers
             sa.attn_fwd_bf16(dq, dk, dv, out=o1, softmax_scale=scale, stream=comp)
+            bf16_done[bf].record(comp)
             sa.sage_attention(dq, dk, dv, softmax_scale=scale, out=o2, workspace=ws_1, stream=comp, **kw)
             comp_done[bf].record(comp)
-            s_out.wait_event(comp_done[bf])
+            # the BF16 output leaves while the Sage call runs, the Sage output after it
+            s_out.wait_event(bf16_done[bf])
             with torch.cuda.stream(s_out):
                 ho1.copy_(o1, non_blocking=True)
+            s_out.wait_event(comp_done[bf])
+            with torch.cuda.stream(s_out):
                 ho2.copy_(o2, non_blocking=True)
                 out_done[bf].record(s_out)
         comp.wait_event(out_done[(n - 1) % 2])
