@@ -6,8 +6,8 @@ request "gfx1201_sage_prepare / gfx1201_sage_attention", Technical Details and
 commit message of gfx1201_sage_attention).  sage_e4m3_encode runs the same
 packing on arbitrary binary32 values, so the conversion is compared here with
 `oracle.e4m3_encode` on every binary32 bit pattern of magnitude up to 448, both
-signs, and on a stride through the rest of the finite range, where both must
-saturate to +-448.  The oracle's encoder is itself pinned against torch's cast on
+signs, on a stride through the rest of the finite range, where both must
+saturate to +-448, and on the special values (infinities, NaN, signed zeros).  The oracle's encoder is itself pinned against torch's cast on
 the same patterns below 448 (tests/test_oracle_prepare.py).
 """
 import numpy as np
@@ -63,3 +63,17 @@ def test_ragged_lengths_and_offsets(cuda_dev):
             o = out.cpu().numpy()
             assert np.array_equal(o[:n], oracle.e4m3_encode(x[off:off + n]))
             assert (o[n:] == 0xAB).all()
+
+
+@pytest.mark.gpu
+def test_special_values(cuda_dev):
+    # +-inf saturate to +-448 like every magnitude beyond it; NaN gives an e4m3 NaN (S.1111.111),
+    # whose sign bit neither side fixes; signed zeros keep their sign
+    x = np.array([np.inf, -np.inf, np.nan, -np.nan, 0.0, -0.0, 448.0, -448.0, 464.0, -464.0], dtype=np.float32)
+    got = sa.e4m3_encode(torch.from_numpy(x).to(cuda_dev)).cpu().numpy()
+    want = oracle.e4m3_encode(x)
+    assert np.array_equal(got[:2], np.array([0x7E, 0xFE], dtype=np.uint8))
+    assert np.array_equal(got[:2], want[:2])
+    assert ((got[2:4] & 0x7F) == 0x7F).all() and ((want[2:4] & 0x7F) == 0x7F).all()
+    assert np.array_equal(got[4:], want[4:])
+    assert np.array_equal(got[4:6], np.array([0x00, 0x80], dtype=np.uint8))
