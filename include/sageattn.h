@@ -449,7 +449,8 @@ ATTN_API attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_strea
  * documents).  It runs the same packing as sage_prepare's V codes and the FP8
  * P of the Sage forward, so the conversion they share can be checked on its
  * own, and serves callers that quantise other tensors the same way.
- *   x : device float32 [n];  y : device uint8 [n], written (any alignment)
+ *   x : device float32 [n];  y : device uint8 [n], written (any alignment); the two
+ *       ranges must not overlap
  *   n : number of values; 0 returns ATTN_OK at once
  * Enqueues one kernel on `stream`.  Errors: n < 0, NULL x or y (n > 0) ->
  * ATTN_ERR_INVALID_ARG; launch failure -> ATTN_ERR_CUDA.
