@@ -45,7 +45,9 @@
  *     returns ATTN_OK at once, writing and reading nothing (its pointers may be NULL).
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
  *     owned by the caller; the library never allocates, frees or keeps them.
- *     Every pointer must be 16-byte aligned.
+ *     Every pointer must be 16-byte aligned (sage_e4m3_encode's arrays need only
+ *     their element alignment).  A call's outputs and workspace must not overlap
+ *     its inputs or one another.
  *   - BF16 tensors are addressed as [B, S, H, 128] with element strides given
  *     as int64_t str[3] = {stride_b, stride_s, stride_h}; the channel stride is
  *     1.  Each stride must be a positive multiple of 8 elements (16 bytes);
@@ -449,8 +451,8 @@ ATTN_API attn_status attn_sm_clock_sample(uint64_t* out, int n_slots, attn_strea
  * documents).  It runs the same packing as sage_prepare's V codes and the FP8
  * P of the Sage forward, so the conversion they share can be checked on its
  * own, and serves callers that quantise other tensors the same way.
- *   x : device float32 [n];  y : device uint8 [n], written (any alignment); the two
- *       ranges must not overlap
+ *   x : device float32 [n] (4-byte aligned);  y : device uint8 [n], written (any
+ *       alignment); the two ranges must not overlap
  *   n : number of values; 0 returns ATTN_OK at once
  * Enqueues one kernel on `stream`.  Errors: n < 0, NULL x or y (n > 0) ->
  * ATTN_ERR_INVALID_ARG; launch failure -> ATTN_ERR_CUDA.
