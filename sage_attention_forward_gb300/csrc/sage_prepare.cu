@@ -216,17 +216,21 @@ __device__ __forceinline__ void group_bar_sync(int group) {
 // warps keep more loads in flight (measured on a GB300: the prepare at Wan-720p 0.80 ->
 // 0.71 ms, at FLUX-2048 with RMSNorm + RoPE 0.30 -> 0.26 ms; four warps of 8 rows at five
 // CTAs per SM was slower at Wan-720p).
-constexpr int kQuantWarpsPerBlock = 2;   // the instance without Q smoothing (1, 2 or 4)
-__host__ __device__ constexpr int quant_blocks_per_cta(bool q_smooth) {
-  return q_smooth ? 8 : 8 / kQuantWarpsPerBlock;
+// Small problems (few blocks per task) take four warps of 8 rows per block instead, at
+// five CTAs per SM: more and shorter CTAs fill the last wave of a small grid better
+// (FLUX-1024, 3456 blocks per task: the one-call Sage op 195 -> 187 us; FLUX-2048 and
+// larger keep two warps, which the larger grids prefer).
+constexpr long long kQuantSmallBlocks = 8192;   // blocks per task (B * H * S_pad / 32) up to this
+__host__ __device__ constexpr int quant_min_ctas(int warps_per_block) {
+  return warps_per_block == 1 ? 1 : (warps_per_block == 2 ? 4 : 5);
 }
 
-// kQSmooth: the instance that smooths Q (its block mean, binary16 mean output)
-template <bool kQSmooth>
-__global__ void __launch_bounds__(256, kQSmooth ? 1 : 4) prep_qk_vmax_kernel(const QKParams p) {
+// kWarpsPerBlock 1: the instance that smooths Q (its block mean, binary16 mean output)
+template <int kWarpsPerBlock>
+__global__ void __launch_bounds__(256, quant_min_ctas(kWarpsPerBlock)) prep_qk_vmax_kernel(const QKParams p) {
   griddep_launch_dependents();   // the next kernel may set up meanwhile (it waits for this grid)
-  constexpr int kBlocksPerCta = quant_blocks_per_cta(kQSmooth);
-  constexpr int kWarpsPerBlock = 8 / kBlocksPerCta;   // 1, 2 or 4
+  constexpr bool kQSmooth = (kWarpsPerBlock == 1);
+  constexpr int kBlocksPerCta = 8 / kWarpsPerBlock;
   constexpr int kSteps = 8 / kWarpsPerBlock;          // rows per lane: 8, 4 or 2
   const int task = blockIdx.z + p.task0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -662,12 +666,15 @@ cudaError_t launch_prepare_heads(const PrepareArgs& a, cudaStream_t stream) {
   const int tasks = (a.skip_v ? 2 : 3) - p.task0;
   if (tasks > 0) {
     const bool q_smooth = p.qmean16 != nullptr && p.task0 == 0;
-    const int per_cta = quant_blocks_per_cta(q_smooth);
+    const int wpb = q_smooth ? 1 : ((long long)BH * nblk <= kQuantSmallBlocks ? 4 : 2);
+    const int per_cta = 8 / wpb;
     dim3 g1((nblk + per_cta - 1) / per_cta, BH, tasks);
-    if (q_smooth)
-      prep_qk_vmax_kernel<true><<<g1, 256, 0, stream>>>(p);
+    if (wpb == 1)
+      prep_qk_vmax_kernel<1><<<g1, 256, 0, stream>>>(p);
+    else if (wpb == 2)
+      prep_qk_vmax_kernel<2><<<g1, 256, 0, stream>>>(p);
     else
-      prep_qk_vmax_kernel<false><<<g1, 256, 0, stream>>>(p);
+      prep_qk_vmax_kernel<4><<<g1, 256, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
