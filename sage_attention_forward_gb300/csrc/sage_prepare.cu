@@ -218,9 +218,9 @@ __device__ __forceinline__ void group_bar_sync(int group) {
 // CTAs per SM was slower at Wan-720p).
 // Small problems (few blocks per task) take four warps of 8 rows per block instead, at
 // five CTAs per SM: more and shorter CTAs fill the last wave of a small grid better
-// (FLUX-1024, 3456 blocks per task: the one-call Sage op 195 -> 187 us; FLUX-2048 and
-// larger keep two warps, which the larger grids prefer).
-constexpr long long kQuantSmallBlocks = 8192;   // blocks per task (B * H * S_pad / 32) up to this
+// (FLUX-1024, 3456 blocks per task: the one-call Sage op 195 -> 187 us; at 8192 blocks the
+// prepare was already 5 % slower that way, and larger grids prefer two warps).
+constexpr long long kQuantSmallBlocks = 4096;   // blocks per task (B * H * S_pad / 32) up to this
 __host__ __device__ constexpr int quant_min_ctas(int warps_per_block) {
   return warps_per_block == 1 ? 1 : (warps_per_block == 2 ? 4 : 5);
 }
