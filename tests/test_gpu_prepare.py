@@ -53,6 +53,17 @@ def test_small_ragged_bit_exact(cuda_dev, B, H, S):
     assert_prepared_equal(prep, exp, f"B{B} H{H} S{S}")
 
 
+@pytest.mark.parametrize("H", [32, 33])
+def test_both_quantiser_layouts_bit_exact(cuda_dev, H):
+    # the quantiser takes four warps per 32-row block up to 4096 blocks per task and two
+    # beyond: S = 4000 pads to 4096 rows, 128 blocks a head, so 32 heads sit exactly at the
+    # bound and 33 just past it; RMSNorm and RoPE on, a ragged last block
+    inp = make_inputs(small_case(1, H, 4000, 4000 + H, rms_norm=True, rope_dim=64))
+    prep, exp = run(inp, cuda_dev)
+    assert prep.S_pad == 4096 and H * prep.S_pad // 32 in (4096, 4224)
+    assert_prepared_equal(prep, exp, f"H={H}")
+
+
 def test_extra_padding_is_zero(cuda_dev):
     inp = make_inputs(small_case(1, 2, 100, 3))
     prep, exp = run(inp, cuda_dev, S_pad=512)
